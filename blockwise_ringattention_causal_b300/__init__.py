@@ -1,0 +1,227 @@
+"""Exact causal, segment-masked (packed) softmax attention for B300 (sm_103a).
+
+A thin ctypes binding over the C ABI of ``liblwm_attn.so`` (declared in
+``include/lwm_attn.h``): the functions below only check and marshal torch tensors
+into pointers and sizes; every step of the computation runs in the library's CUDA
+kernels. There is no CPU fallback: without the built library every call raises.
+
+Attention computed (LWM, "World Model on Million-Length Video And Language With
+Blockwise RingAttention"; deep-dive page, sections "RingAttention 为什么必要",
+"模型结构" and "Masked sequence packing"): exact softmax(q k^T / sqrt(D)) v, causal,
+with several documents packed in one row attending only to themselves.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "LwmError", "library_path", "load_library",
+    "lwm_attn_workspace_size", "lwm_attn_prepare", "lwm_attn_fwd", "lwm_attn_fwd_ring",
+    "lwm_attn_fwd_prepared", "lwm_attn_bwd", "lwm_attn_bwd_prepared", "lwm_attn_check",
+    "lwm_status_string", "new_workspace", "forward", "backward",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+STATUS_NAMES = {
+    0: "LWM_OK", 1: "LWM_ERR_INVALID_ARG", 2: "LWM_ERR_UNSUPPORTED", 3: "LWM_ERR_ALIGNMENT",
+    4: "LWM_ERR_SEGMENTS", 5: "LWM_ERR_WORKSPACE", 6: "LWM_ERR_CUDA", 7: "LWM_ERR_TIMEOUT",
+}
+
+# name -> (restype, argtypes)
+_P, _I, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_SIGNATURES = {
+    "lwm_attn_workspace_size": (_Z, [_I, _I, _I, _I]),
+    "lwm_attn_prepare": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lwm_attn_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
+    "lwm_attn_fwd_ring": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lwm_attn_fwd_prepared": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
+    "lwm_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
+    "lwm_attn_bwd_prepared": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
+    "lwm_attn_check": (_I, [_P, _P]),
+    "lwm_status_string": (ctypes.c_char_p, [_I]),
+}
+
+
+class LwmError(RuntimeError):
+    """A non-zero lwm_status returned by the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lwm_status_string(status)}")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "liblwm_attn.so")
+
+
+def load_library():
+    """Load liblwm_attn.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m blockwise_ringattention_causal_b300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def lwm_status_string(status: int) -> str:
+    try:
+        return load_library().lwm_status_string(int(status)).decode()
+    except RuntimeError:
+        return STATUS_NAMES.get(int(status), f"status {status}")
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise LwmError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected a [B, S, H, D] tensor")
+    return tuple(int(x) for x in q.shape)
+
+
+def _need(t, name, dtype, shape=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _seg(seg, pos, B, S):
+    for t, n in ((seg, "seg_ids"), (pos, "pos")):
+        if t is not None:
+            _need(t, n, torch.int32, (B, S))
+
+
+def lwm_attn_workspace_size(B, S, H, D) -> int:
+    return int(load_library().lwm_attn_workspace_size(B, S, H, D))
+
+
+def new_workspace(B, S, H, D, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace (the library requires zeros before first use)."""
+    n = lwm_attn_workspace_size(B, S, H, D)
+    if n == 0:
+        raise ValueError("unsupported sizes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def lwm_attn_prepare(seg_ids, pos, B, S, H, D, kv_chunks, workspace, stream=None):
+    _seg(seg_ids, pos, B, S)
+    _check(load_library().lwm_attn_prepare(_ptr(seg_ids), _ptr(pos), B, S, H, D, kv_chunks,
+                                           _ptr(workspace), workspace.numel(), _stream(stream)),
+           "lwm_attn_prepare")
+
+
+def lwm_attn_fwd(q, k, v, seg_ids, pos, out, lse, workspace, stream=None):
+    B, S, H, D = _shape(q)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.bfloat16, (B, S, H, D))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    _seg(seg_ids, pos, B, S)
+    _check(load_library().lwm_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(seg_ids), _ptr(pos), _ptr(out),
+                                       _ptr(lse), B, S, H, D, _ptr(workspace), workspace.numel(),
+                                       _stream(stream)), "lwm_attn_fwd")
+
+
+def lwm_attn_fwd_ring(q, k, v, seg_ids, pos, out, lse, kv_chunks, workspace, stream=None):
+    B, S, H, D = _shape(q)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.bfloat16, (B, S, H, D))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    _seg(seg_ids, pos, B, S)
+    _check(load_library().lwm_attn_fwd_ring(_ptr(q), _ptr(k), _ptr(v), _ptr(seg_ids), _ptr(pos), _ptr(out),
+                                            _ptr(lse), B, S, H, D, int(kv_chunks), _ptr(workspace),
+                                            workspace.numel(), _stream(stream)), "lwm_attn_fwd_ring")
+
+
+def lwm_attn_fwd_prepared(q, k, v, out, lse, workspace, stream=None):
+    B, S, H, D = _shape(q)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.bfloat16, (B, S, H, D))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    _check(load_library().lwm_attn_fwd_prepared(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, D,
+                                                _ptr(workspace), workspace.numel(), _stream(stream)),
+           "lwm_attn_fwd_prepared")
+
+
+def lwm_attn_bwd(q, k, v, out, dout, lse, seg_ids, pos, dq, dk, dv, workspace, stream=None):
+    B, S, H, D = _shape(q)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"), (dk, "dk"),
+                 (dv, "dv")):
+        _need(t, n, torch.bfloat16, (B, S, H, D))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    _seg(seg_ids, pos, B, S)
+    _check(load_library().lwm_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                       _ptr(seg_ids), _ptr(pos), _ptr(dq), _ptr(dk), _ptr(dv), B, S, H, D,
+                                       _ptr(workspace), workspace.numel(), _stream(stream)), "lwm_attn_bwd")
+
+
+def lwm_attn_bwd_prepared(q, k, v, out, dout, lse, dq, dk, dv, workspace, stream=None):
+    B, S, H, D = _shape(q)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"), (dk, "dk"),
+                 (dv, "dv")):
+        _need(t, n, torch.bfloat16, (B, S, H, D))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    _check(load_library().lwm_attn_bwd_prepared(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                                _ptr(dq), _ptr(dk), _ptr(dv), B, S, H, D, _ptr(workspace),
+                                                workspace.numel(), _stream(stream)), "lwm_attn_bwd_prepared")
+
+
+def lwm_attn_check(workspace, stream=None) -> int:
+    """Synchronise and return (and clear) the device error status; 0 = LWM_OK."""
+    return int(load_library().lwm_attn_check(_ptr(workspace), _stream(stream)))
+
+
+def forward(q, k, v, seg_ids=None, pos=None, kv_chunks=1, workspace=None, stream=None):
+    """Allocate out/lse and run the forward pass. Returns (out, lse, workspace)."""
+    B, S, H, D = _shape(q)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = new_workspace(B, S, H, D, q.device)
+    if kv_chunks == 1:
+        lwm_attn_fwd(q, k, v, seg_ids, pos, out, lse, workspace, stream)
+    else:
+        lwm_attn_fwd_ring(q, k, v, seg_ids, pos, out, lse, kv_chunks, workspace, stream)
+    return out, lse, workspace
+
+
+def backward(q, k, v, out, dout, lse, seg_ids=None, pos=None, workspace=None, stream=None):
+    """Allocate dq/dk/dv and run the backward pass. Returns (dq, dk, dv)."""
+    B, S, H, D = _shape(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = new_workspace(B, S, H, D, q.device)
+    lwm_attn_bwd(q, k, v, out, dout, lse, seg_ids, pos, dq, dk, dv, workspace, stream)
+    return dq, dk, dv

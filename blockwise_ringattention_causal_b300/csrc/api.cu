@@ -1,0 +1,248 @@
+// C ABI of the attention library: argument checks, TMA tensor maps and kernel
+// launches. See include/lwm_attn.h for the contract of every entry point.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lwm {
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+struct DeviceInfo {
+  bool known = false;
+  bool supported = false;
+  int num_sms = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[MAX_DEVICES];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+lwm_status device_info(DeviceInfo &out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return LWM_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (!d.known) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return LWM_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);   // the kernels are built for sm_103a
+    d.num_sms = sms;
+    d.known = true;
+  }
+  if (!g_encode) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return LWM_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  out = d;
+  return d.supported ? LWM_OK : LWM_ERR_UNSUPPORTED;
+}
+
+// [B, S, H, 128] bf16, loaded as boxes of 64 dims x 1 head x 128 rows x 1 batch row,
+// 128-byte swizzled (the K-major / MN-major canonical layout of the MMA operands).
+bool make_map(CUtensorMap *m, const void *ptr, int B, int S, int H) {
+  cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(H), cuuint64_t(S), cuuint64_t(B)};
+  cuuint64_t strides[3] = {cuuint64_t(HD) * 2, cuuint64_t(H) * HD * 2, cuuint64_t(S) * H * HD * 2};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+lwm_status check_sizes(int B, int S, int H, int D) {
+  if (B <= 0 || S <= 0 || H <= 0 || D <= 0) return LWM_ERR_INVALID_ARG;
+  if (D != HD) return LWM_ERR_UNSUPPORTED;
+  const long long nT = (S + BM - 1) / BM;
+  if (static_cast<long long>(B) * S >= (1ll << 31)) return LWM_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * ((nT + 1) / 2) * H >= (1ll << 31)) return LWM_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * nT * H >= (1ll << 31)) return LWM_ERR_INVALID_ARG;
+  return LWM_OK;
+}
+
+lwm_status check_workspace(const void *ws, size_t bytes, int B, int S, int H) {
+  if (!ws) return LWM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LWM_ERR_WORKSPACE;
+  if (bytes < Workspace::layout(B, S, H).total) return LWM_ERR_INVALID_ARG;
+  return LWM_OK;
+}
+
+lwm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LWM_OK : LWM_ERR_CUDA; }
+
+#define LWM_TRY(x)                 \
+  do {                             \
+    const lwm_status s_ = (x);     \
+    if (s_ != LWM_OK) return s_;   \
+  } while (0)
+
+lwm_status prepare_impl(const int32_t *seg, const int32_t *pos, int B, int S, int H, int kv_chunks, void *ws,
+                        cudaStream_t stream) {
+  const int nT = (S + BM - 1) / BM;
+  int chunk_tiles = (nT + kv_chunks - 1) / kv_chunks;
+  if (chunk_tiles < 1) chunk_tiles = 1;
+  return from_cuda(launch_meta(seg, pos, B, S, chunk_tiles, ws, stream));
+}
+
+lwm_status fwd_common(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, lwm_bf16 *out, float *lse,
+                      int B, int S, int H, void *ws, cudaStream_t stream, const DeviceInfo &d) {
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, B, S, H) || !make_map(&tk, k, B, S, H) || !make_map(&tv, v, B, S, H))
+    return LWM_ERR_CUDA;
+  Problem p{B, S, H, d.num_sms};
+  return from_cuda(launch_fwd(tq, tk, tv, out, lse, p, ws, stream));
+}
+
+lwm_status check_fwd_args(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, lwm_bf16 *out, float *lse,
+                          int B, int S, int H, int D, void *ws, size_t ws_bytes) {
+  LWM_TRY(check_sizes(B, S, H, D));
+  if (!q || !k || !v || !out || !lse) return LWM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned4(lse))
+    return LWM_ERR_ALIGNMENT;
+  return check_workspace(ws, ws_bytes, B, S, H);
+}
+
+lwm_status check_seg_args(const int32_t *seg, const int32_t *pos) {
+  if ((seg && !aligned4(seg)) || (pos && !aligned4(pos))) return LWM_ERR_ALIGNMENT;
+  return LWM_OK;
+}
+
+lwm_status check_bwd_args(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,
+                          const lwm_bf16 *dout, const float *lse, lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv, int B,
+                          int S, int H, int D, void *ws, size_t ws_bytes) {
+  LWM_TRY(check_sizes(B, S, H, D));
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return LWM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse))
+    return LWM_ERR_ALIGNMENT;
+  return check_workspace(ws, ws_bytes, B, S, H);
+}
+
+lwm_status bwd_common(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,
+                      const lwm_bf16 *dout, const float *lse, lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv, int B,
+                      int S, int H, void *ws, cudaStream_t stream, const DeviceInfo &d) {
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(&tq, q, B, S, H) || !make_map(&tk, k, B, S, H) || !make_map(&tv, v, B, S, H) ||
+      !make_map(&tdo, dout, B, S, H))
+    return LWM_ERR_CUDA;
+  Problem p{B, S, H, d.num_sms};
+  LWM_TRY(from_cuda(launch_delta(out, dout, lse, p, ws, stream)));
+  LWM_TRY(from_cuda(launch_dkdv(tq, tk, tv, tdo, dk, dv, p, ws, stream)));
+  return from_cuda(launch_dq(tq, tk, tv, tdo, dq, p, ws, stream));
+}
+
+}  // namespace
+}  // namespace lwm
+
+using namespace lwm;
+
+extern "C" {
+
+size_t lwm_attn_workspace_size(int B, int S, int H, int D) {
+  if (check_sizes(B, S, H, D) != LWM_OK) return 0;
+  return Workspace::layout(B, S, H).total;
+}
+
+lwm_status lwm_attn_prepare(const int32_t *seg_ids, const int32_t *pos, int B, int S, int H, int D,
+                            int kv_chunks, void *workspace, size_t workspace_bytes, lwm_stream stream) {
+  LWM_TRY(check_sizes(B, S, H, D));
+  if (kv_chunks < 1) return LWM_ERR_INVALID_ARG;
+  LWM_TRY(check_seg_args(seg_ids, pos));
+  LWM_TRY(check_workspace(workspace, workspace_bytes, B, S, H));
+  DeviceInfo d;
+  LWM_TRY(device_info(d));
+  return prepare_impl(seg_ids, pos, B, S, H, kv_chunks, workspace, stream);
+}
+
+lwm_status lwm_attn_fwd_ring(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const int32_t *seg_ids,
+                             const int32_t *pos, lwm_bf16 *out, float *lse, int B, int S, int H, int D,
+                             int kv_chunks, void *workspace, size_t workspace_bytes, lwm_stream stream) {
+  LWM_TRY(check_fwd_args(q, k, v, out, lse, B, S, H, D, workspace, workspace_bytes));
+  if (kv_chunks < 1) return LWM_ERR_INVALID_ARG;
+  LWM_TRY(check_seg_args(seg_ids, pos));
+  DeviceInfo d;
+  LWM_TRY(device_info(d));
+  LWM_TRY(prepare_impl(seg_ids, pos, B, S, H, kv_chunks, workspace, stream));
+  return fwd_common(q, k, v, out, lse, B, S, H, workspace, stream, d);
+}
+
+lwm_status lwm_attn_fwd(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const int32_t *seg_ids,
+                        const int32_t *pos, lwm_bf16 *out, float *lse, int B, int S, int H, int D, void *workspace,
+                        size_t workspace_bytes, lwm_stream stream) {
+  return lwm_attn_fwd_ring(q, k, v, seg_ids, pos, out, lse, B, S, H, D, 1, workspace, workspace_bytes, stream);
+}
+
+lwm_status lwm_attn_fwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, lwm_bf16 *out,
+                                 float *lse, int B, int S, int H, int D, void *workspace, size_t workspace_bytes,
+                                 lwm_stream stream) {
+  LWM_TRY(check_fwd_args(q, k, v, out, lse, B, S, H, D, workspace, workspace_bytes));
+  DeviceInfo d;
+  LWM_TRY(device_info(d));
+  return fwd_common(q, k, v, out, lse, B, S, H, workspace, stream, d);
+}
+
+lwm_status lwm_attn_bwd(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,
+                        const lwm_bf16 *dout, const float *lse, const int32_t *seg_ids, const int32_t *pos,
+                        lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv, int B, int S, int H, int D, void *workspace,
+                        size_t workspace_bytes, lwm_stream stream) {
+  LWM_TRY(check_bwd_args(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, D, workspace, workspace_bytes));
+  LWM_TRY(check_seg_args(seg_ids, pos));
+  DeviceInfo d;
+  LWM_TRY(device_info(d));
+  LWM_TRY(prepare_impl(seg_ids, pos, B, S, H, 1, workspace, stream));
+  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, workspace, stream, d);
+}
+
+lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,
+                                 const lwm_bf16 *dout, const float *lse, lwm_bf16 *dq, lwm_bf16 *dk,
+                                 lwm_bf16 *dv, int B, int S, int H, int D, void *workspace,
+                                 size_t workspace_bytes, lwm_stream stream) {
+  LWM_TRY(check_bwd_args(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, D, workspace, workspace_bytes));
+  DeviceInfo d;
+  LWM_TRY(device_info(d));
+  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, workspace, stream, d);
+}
+
+lwm_status lwm_attn_check(void *workspace, lwm_stream stream) {
+  if (!workspace) return LWM_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return LWM_ERR_CUDA;
+  int word = 0;
+  int *hdr = static_cast<int *>(workspace);
+  if (cudaMemcpy(&word, hdr + HDR_ERR, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LWM_ERR_CUDA;
+  if (word != 0 && cudaMemset(hdr + HDR_ERR, 0, sizeof(int)) != cudaSuccess) return LWM_ERR_CUDA;
+  if (word & ERRBIT_SEGMENTS) return LWM_ERR_SEGMENTS;
+  if (word & ERRBIT_TIMEOUT) return LWM_ERR_TIMEOUT;
+  return LWM_OK;
+}
+
+const char *lwm_status_string(lwm_status status) {
+  switch (status) {
+    case LWM_OK: return "LWM_OK";
+    case LWM_ERR_INVALID_ARG: return "LWM_ERR_INVALID_ARG: null pointer, bad size or too-small workspace";
+    case LWM_ERR_UNSUPPORTED: return "LWM_ERR_UNSUPPORTED: only D == 128 on sm_103 devices";
+    case LWM_ERR_ALIGNMENT: return "LWM_ERR_ALIGNMENT: tensors must be 16-byte aligned";
+    case LWM_ERR_SEGMENTS: return "LWM_ERR_SEGMENTS: seg_ids/pos break the packing preconditions";
+    case LWM_ERR_WORKSPACE: return "LWM_ERR_WORKSPACE: workspace must be 256-byte aligned";
+    case LWM_ERR_CUDA: return "LWM_ERR_CUDA: a CUDA call failed";
+    case LWM_ERR_TIMEOUT: return "LWM_ERR_TIMEOUT: a device pipeline wait exceeded its bound";
+  }
+  return "unknown lwm_status";
+}
+
+}  // extern "C"

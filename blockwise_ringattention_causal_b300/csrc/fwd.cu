@@ -1,0 +1,525 @@
+// Forward pass: exact causal, segment-masked softmax attention, block by block with an
+// online softmax, on the sm_100-family tensor cores (tcgen05 + TMEM) with TMA-staged
+// tiles.
+//
+// Method (LWM, "World Model on Million-Length Video And Language With Blockwise
+// RingAttention"; deep-dive page, section "RingAttention 为什么必要"): exact attention
+// computed block by block, so that memory stays linear in the sequence length. The
+// per-block normaliser is the running max / running sum of the blockwise-transformer
+// work the pages cite by title. On one GPU the ring of devices becomes the loop over
+// key/value tiles below; kv_chunks > 1 visits the tiles in ring order.
+//
+// One persistent CTA per SM takes work items (b, h, pair of 128-row query tiles) from
+// a longest-first list through an atomic ticket. Warp roles:
+//   warps 0-3  softmax for query tile 0 (one TMEM lane = one query row per thread)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer (and the scheduler ticket)
+//   warp  9    tcgen05 MMA issuer (and TMEM owner)
+// TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P (bf16) is written
+// over the first 64 columns of its S. MMA order per key tile j:
+//   S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
+// so that one softmax warpgroup works while the tensor core serves the other.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lwm {
+namespace {
+
+constexpr int FWD_WARPS = 10;
+constexpr int FWD_THREADS = FWD_WARPS * 32;
+constexpr int WARP_PRODUCER = 8;
+constexpr int WARP_MMA = 9;
+constexpr int KV_STAGES = 4;
+
+constexpr int SM_Q = 0;
+constexpr int SM_KV = 2 * TILE_BYTES;
+constexpr int SM_BAR = SM_KV + KV_STAGES * TILE_BYTES;
+
+struct FwdBars {
+  uint64_t kv_full[KV_STAGES], kv_empty[KV_STAGES];
+  uint64_t q_full, q_empty;
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t item_full[2], item_empty[2];
+  uint64_t drain;
+  int item[2];
+  uint32_t tmem_base;
+  int abort;
+  int kv_fill, kv_use, q_issued, q_used;
+};
+
+constexpr int FWD_SMEM = SM_BAR + int(sizeof(FwdBars)) + 1024;   // + alignment slack
+
+__device__ __forceinline__ uint32_t col_s(int t) { return t ? 128u : 0u; }   // S_t (and P_t)
+__device__ __forceinline__ uint32_t col_o(int t) { return t ? 384u : 256u; }  // O_t
+constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);   // Q, K both K-major
+constexpr uint32_t IDESC_PV = idesc_bf16(BM, HD, false, true);    // P from TMEM, V MN-major
+constexpr float NEG_INF = -__builtin_huge_valf();
+
+struct FwdArgs {
+  const int *lo;
+  const int *list;
+  int *hdr;
+  __nv_bfloat16 *out;
+  float *lse;
+  int B, S, H, nP, n_items;
+  float scale_log2;   // log2(e) / sqrt(D)
+};
+
+struct Item {
+  int b, h, pair;
+};
+
+__device__ __forceinline__ Item decode(const FwdArgs &a, int item) {
+  const int e = a.list[item / a.H];
+  return {e / a.nP, item % a.H, e % a.nP};
+}
+
+// S = Q K^T over D = 128: 8 MMAs of K = 16; each 64-dim half of a tile is one
+// 128B-swizzled K-major block (rows 128 bytes apart, 8-row groups 1024 bytes apart).
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_s, uint32_t k_s) {
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    const uint32_t off = uint32_t(kk >> 2) * HALF_BYTES + uint32_t(kk & 3) * 32;
+    mma_ss(d_tmem, sdesc_sw128(q_s + off, 16, 1024), sdesc_sw128(k_s + off, 16, 1024), IDESC_QK, kk > 0);
+  }
+}
+
+// O (+)= P V over 128 keys: 8 MMAs of K = 16 keys; V is MN-major (dims contiguous):
+// 16 keys = two 1024-byte 8-row groups; the two 64-dim halves are HALF_BYTES apart.
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_s, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk) {
+    mma_ts(o_tmem, p_tmem + uint32_t(kk) * 8, sdesc_sw128(v_s + uint32_t(kk) * 2048, HALF_BYTES, 1024),
+           IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+struct Ranges {
+  TileRange r[2];
+  int first, last;
+};
+
+__device__ __forceinline__ Ranges item_ranges(const FwdArgs &a, const Item &I) {
+  const int *lr = a.lo + size_t(I.b) * a.S;
+  Ranges R;
+  R.r[0] = q_tile_kv_range(lr, a.S, (2 * I.pair) * BM);
+  R.r[1] = q_tile_kv_range(lr, a.S, (2 * I.pair + 1) * BM);
+  if (R.r[0].empty()) {
+    R.first = R.r[1].first;
+    R.last = R.r[1].last;
+  } else if (R.r[1].empty()) {
+    R.first = R.r[0].first;
+    R.last = R.r[0].last;
+  } else {
+    R.first = min(R.r[0].first, R.r[1].first);
+    R.last = max(R.r[0].last, R.r[1].last);
+  }
+  return R;
+}
+
+// ----------------------------------------------------------------------------- producer
+__device__ bool producer_role(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
+                              const FwdArgs &a, uint8_t *smem, FwdBars *bars, int kv_chunk) {
+  volatile int *abort = &bars->abort;
+  int kv_fill = 0, q_issued = 0;
+  bool ok = true;
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_empty[slot], ((it >> 1) & 1) ^ 1, abort))) break;
+    const int t = atomicAdd(a.hdr + HDR_TICKET_FWD, 1);
+    const int item = t < a.n_items ? t : -1;
+    bars->item[slot] = item;
+    mbar_arrive(&bars->item_full[slot]);
+    if (item < 0) break;
+    const Item I = decode(a, item);
+    const Ranges R = item_ranges(a, I);
+    if (!(ok = mbar_wait(&bars->q_empty, (it & 1) ^ 1, abort))) break;
+    const int q0 = 2 * I.pair * BM;
+    mbar_arrive_expect_tx(&bars->q_full, 2 * TILE_BYTES);
+    tma_load_4d(tq, &bars->q_full, smem + SM_Q, 0, I.h, q0, I.b);
+    tma_load_4d(tq, &bars->q_full, smem + SM_Q + HALF_BYTES, 64, I.h, q0, I.b);
+    tma_load_4d(tq, &bars->q_full, smem + SM_Q + TILE_BYTES, 0, I.h, q0 + BM, I.b);
+    tma_load_4d(tq, &bars->q_full, smem + SM_Q + TILE_BYTES + HALF_BYTES, 64, I.h, q0 + BM, I.b);
+    ++q_issued;
+    KvSeq seq;
+    for (seq.init(R.first, R.last, kv_chunk); seq.valid() && ok; seq.next()) {
+      for (int w = 0; w < 2; ++w) {
+        const int st = kv_fill % KV_STAGES;
+        if (!(ok = mbar_wait(&bars->kv_empty[st], ((kv_fill / KV_STAGES) & 1) ^ 1, abort))) break;
+        mbar_arrive_expect_tx(&bars->kv_full[st], TILE_BYTES);
+        const CUtensorMap *m = w ? tv : tk;
+        uint8_t *dst = smem + SM_KV + st * TILE_BYTES;
+        tma_load_4d(m, &bars->kv_full[st], dst, 0, I.h, seq.t * BN, I.b);
+        tma_load_4d(m, &bars->kv_full[st], dst + HALF_BYTES, 64, I.h, seq.t * BN, I.b);
+        ++kv_fill;
+      }
+    }
+    if (!ok) break;
+  }
+  bars->kv_fill = kv_fill;
+  bars->q_issued = q_issued;
+  return ok;
+}
+
+// ----------------------------------------------------------------------------- MMA issuer
+__device__ bool mma_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_t tmem, int kv_chunk,
+                         int lane) {
+  volatile int *abort = &bars->abort;
+  const uint32_t q_s[2] = {smem_u32(smem + SM_Q), smem_u32(smem + SM_Q + TILE_BYTES)};
+  const uint32_t kv_s0 = smem_u32(smem + SM_KV);
+  int kv_use = 0, q_used = 0;
+  uint32_t pf_par[2] = {0, 0}, oe_par[2] = {1, 1};
+  bool ok = true;
+
+  auto wait_kv = [&](int &st) -> bool {
+    st = kv_use % KV_STAGES;
+    const bool r = mbar_wait(&bars->kv_full[st], (kv_use / KV_STAGES) & 1, abort);
+    ++kv_use;
+    tc_fence_after();
+    return r;
+  };
+
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
+    const int item = bars->item[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+    if (item < 0) break;
+    const Item I = decode(a, item);
+    const Ranges R = item_ranges(a, I);
+    if (!(ok = mbar_wait(&bars->q_full, it & 1, abort))) break;
+    ++q_used;
+    tc_fence_after();
+    bool first[2] = {true, true};
+    KvSeq seq;
+    seq.init(R.first, R.last, kv_chunk);
+    if (seq.valid()) {
+      int stK;
+      if (!(ok = wait_kv(stK))) break;
+      if (lane == 0) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (R.r[t].has(seq.t)) {
+            issue_qk(tmem + col_s(t), q_s[t], kv_s0 + stK * TILE_BYTES);
+            mma_commit(&bars->s_full[t]);
+          }
+        mma_commit(&bars->kv_empty[stK]);
+      }
+      __syncwarp();
+      while (ok) {
+        const int cur = seq.t;
+        int stV;
+        if (!(ok = wait_kv(stV))) break;
+        seq.next();
+        const bool has_next = seq.valid();
+        const int nxt = seq.t;
+        int stK2 = -1;
+#pragma unroll
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (R.r[t].has(cur)) {
+            if (first[t]) {
+              if (!(ok = mbar_wait(&bars->o_empty[t], oe_par[t], abort))) break;
+              oe_par[t] ^= 1;
+            }
+            if (!(ok = mbar_wait(&bars->p_full[t], pf_par[t], abort))) break;
+            pf_par[t] ^= 1;
+            tc_fence_after();
+            if (lane == 0) issue_pv(tmem + col_o(t), tmem + col_s(t), kv_s0 + stV * TILE_BYTES, !first[t]);
+            first[t] = false;
+          }
+          if (has_next) {
+            if (t == 0 && !(ok = wait_kv(stK2))) break;
+            if (lane == 0 && R.r[t].has(nxt)) {
+              issue_qk(tmem + col_s(t), q_s[t], kv_s0 + stK2 * TILE_BYTES);
+              mma_commit(&bars->s_full[t]);
+            }
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          if (has_next) mma_commit(&bars->kv_empty[stK2]);
+          mma_commit(&bars->kv_empty[stV]);
+        }
+        __syncwarp();
+        if (!has_next) break;
+      }
+      if (!ok) break;
+    }
+    if (lane == 0) {
+      mma_commit(&bars->q_empty);
+      if (!first[0]) mma_commit(&bars->o_full[0]);
+      if (!first[1]) mma_commit(&bars->o_full[1]);
+    }
+    __syncwarp();
+  }
+  if (lane == 0) {
+    bars->kv_use = kv_use;
+    bars->q_used = q_used;
+  }
+  return ok;
+}
+
+// ----------------------------------------------------------------------------- softmax
+__device__ bool softmax_role(const FwdArgs &a, FwdBars *bars, uint32_t tmem, int kv_chunk, int t, int warp,
+                             int lane) {
+  volatile int *abort = &bars->abort;
+  const int wq = warp & 3;
+  const int r = wq * 32 + lane;
+  const uint32_t lane_off = uint32_t(wq * 32) << 16;
+  const uint32_t tS = tmem + lane_off + col_s(t);
+  const uint32_t tO = tmem + lane_off + col_o(t);
+  const float c = a.scale_log2;
+  uint32_t sf_par = 0, of_par = 0;
+  bool ok = true;
+
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
+    const int item = bars->item[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+    if (item < 0) break;
+    const Item I = decode(a, item);
+    const Ranges R = item_ranges(a, I);
+    const TileRange my = R.r[t];
+    const int q0 = (2 * I.pair + t) * BM;
+    const int i = q0 + r;
+    const int *lr = a.lo + size_t(I.b) * a.S;
+    const int lo_i = i < a.S ? lr[i] : i + 1;
+    const int qb = min(q0 + BM, a.S) - 1;
+    const int lo_qb = q0 < a.S ? lr[qb] : 0;
+    float m = NEG_INF, l = 0.f;
+    bool had = false;
+
+    KvSeq seq;
+    for (seq.init(R.first, R.last, kv_chunk); seq.valid(); seq.next()) {
+      const int kt = seq.t;
+      if (!my.has(kt)) continue;
+      if (!(ok = mbar_wait(&bars->s_full[t], sf_par, abort))) break;
+      sf_par ^= 1;
+      tc_fence_after();
+      uint32_t s[BN];
+      tmem_ld32(tS + 0, s);
+      tmem_ld32(tS + 32, s + 32);
+      tmem_ld32(tS + 64, s + 64);
+      tmem_ld32(tS + 96, s + 96);
+      tmem_ld_wait();
+      const int k0 = kt * BN;
+      const bool full = (lo_qb <= k0) && (k0 + BN - 1 <= q0);
+      if (!full) {
+#pragma unroll
+        for (int cc = 0; cc < BN; ++cc) {
+          const int j = k0 + cc;
+          if (j < lo_i || j > i) s[cc] = 0xff800000u;   // -inf
+        }
+      }
+      float mx = NEG_INF;
+#pragma unroll
+      for (int cc = 0; cc < BN; ++cc) mx = fmaxf(mx, __uint_as_float(s[cc]));
+      const float m_new = fmaxf(m, mx * c);
+      // Rescale only when the running max grew by more than 8 (log2 units); otherwise
+      // keep the stale max: p <= 2^8 stays exact in fp32 and the final o = O / l uses
+      // the same max for O and l.
+      const bool resc = m_new > m + 8.f;
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2_approx(m - m_new);   // 0 when m = -inf
+        m = m_new;
+      }
+      const bool fix_o = resc && had && l > 0.f;
+      l *= alpha;
+      if (__any_sync(0xffffffffu, fix_o)) {
+        const float f = fix_o ? alpha : 1.f;
+#pragma unroll
+        for (int cc = 0; cc < HD; cc += 16) {
+          uint32_t o[16];
+          tmem_ld16(tO + cc, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+          tmem_st16(tO + cc, o);
+        }
+      }
+      const float m_use = (m == NEG_INF) ? 0.f : m;
+      float rs = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < BN; cc += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s[cc + 2 * e]), c, -m_use));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s[cc + 2 * e + 1]), c, -m_use));
+          rs += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + cc / 2, pk);
+      }
+      l += rs;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[t]);
+      had = true;
+    }
+    if (!ok) break;
+
+    const size_t orow = (size_t(I.b) * a.S + i) * a.H + I.h;
+    if (had) {
+      if (!(ok = mbar_wait(&bars->o_full[t], of_par, abort))) break;
+      of_par ^= 1;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int cc = 0; cc < HD; cc += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + cc, o);
+        tmem_ld_wait();
+        uint4 w[4];
+        uint32_t *wp = reinterpret_cast<uint32_t *>(w);
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          wp[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+        if (i < a.S) {
+          uint4 *dst = reinterpret_cast<uint4 *>(a.out + orow * HD + cc);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = w[e];
+        }
+      }
+      if (i < a.S) a.lse[(size_t(I.b) * a.H + I.h) * a.S + i] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_empty[t]);
+    } else if (i < a.S) {
+      uint4 *dst = reinterpret_cast<uint4 *>(a.out + orow * HD);
+#pragma unroll
+      for (int e = 0; e < HD / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+      a.lse[(size_t(I.b) * a.H + I.h) * a.S + i] = NEG_INF;
+    }
+  }
+  return ok;
+}
+
+__device__ bool bounded_wait_plain(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+  return true;
+}
+
+__global__ void __maxnreg__(200)
+    fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  FwdBars *bars = reinterpret_cast<FwdBars *>(smem + SM_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kv_chunk = a.hdr[HDR_KV_CHUNK];
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < KV_STAGES; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 4);
+      mbar_init(&bars->o_full[t], 1);
+      mbar_init(&bars->o_empty[t], 4);
+      mbar_init(&bars->item_full[t], 1);
+      mbar_init(&bars->item_empty[t], 9);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    bars->kv_fill = bars->kv_use = bars->q_issued = bars->q_used = 0;
+    fence_mbar_init();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == WARP_PRODUCER && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  bool ok = true;
+  if (warp == WARP_PRODUCER) {
+    if (lane == 0) ok = producer_role(&tq, &tk, &tv, a, smem, bars, kv_chunk);
+    __syncwarp();
+  } else if (warp == WARP_MMA) {
+    ok = mma_role(a, smem, bars, tmem, kv_chunk, lane);
+  } else {
+    ok = softmax_role(a, bars, tmem, kv_chunk, warp >> 2, warp, lane);
+  }
+  if (!ok) {
+    bars->abort = 1;
+    raise_error(a.hdr + HDR_ERR, ERRBIT_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (bars->abort) {
+    // Let copies and MMAs still in flight land before shared memory and TMEM go away.
+    if (warp == WARP_PRODUCER && lane == 0) {
+      for (int n = bars->kv_use; n < bars->kv_fill; ++n)
+        bounded_wait_plain(&bars->kv_full[n % KV_STAGES], (n / KV_STAGES) & 1);
+      if (bars->q_issued > bars->q_used) bounded_wait_plain(&bars->q_full, (bars->q_issued - 1) & 1);
+    }
+    if (warp == WARP_MMA && lane == 0) {
+      mma_commit(&bars->drain);
+      bounded_wait_plain(&bars->drain, 0);
+    }
+    __syncthreads();
+  }
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int d = atomicAdd(a.hdr + HDR_DONE_FWD, 1);
+    if (d == int(gridDim.x) - 1) {
+      a.hdr[HDR_TICKET_FWD] = 0;
+      a.hdr[HDR_DONE_FWD] = 0;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, void *out,
+                       float *lse, const Problem &p, void *workspace, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const Workspace w = Workspace::layout(p.B, p.S, p.H);
+  char *base = static_cast<char *>(workspace);
+  FwdArgs a;
+  a.lo = reinterpret_cast<const int *>(base + w.off_lo);
+  a.list = reinterpret_cast<const int *>(base + w.off_list_fwd);
+  a.hdr = reinterpret_cast<int *>(base + w.off_hdr);
+  a.out = static_cast<__nv_bfloat16 *>(out);
+  a.lse = lse;
+  a.B = p.B;
+  a.S = p.S;
+  a.H = p.H;
+  a.nP = w.nP;
+  a.n_items = p.B * w.nP * p.H;
+  a.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
+  const int grid = a.n_items < p.num_sms ? a.n_items : p.num_sms;
+  fwd_kernel<<<grid, FWD_THREADS, FWD_SMEM, stream>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace lwm

@@ -1,0 +1,138 @@
+/*
+ * lwm_attn.h - C ABI for exact causal, segment-masked (packed) softmax attention on
+ * NVIDIA B300 (sm_103a).
+ *
+ * What is computed. The operation is the attention primitive of "World Model on
+ * Million-Length Video And Language With Blockwise RingAttention" (LWM), as the
+ * charles2530.github.io deep-dive page describes it:
+ *   - section "RingAttention 为什么必要": exact full attention (no window, no sparse
+ *     approximation), computed block by block so that memory stays linear in S;
+ *   - section "模型结构": next-token prediction, hence causal attention;
+ *   - section "Masked sequence packing": several documents share one packed row and
+ *     an attention mask lets each attend only to itself.
+ * For batch row b, head h and query i (0-based), with seg = seg_ids[b, :]:
+ *     visible(i)  = { j : seg[j] == seg[i] >= 0 and j <= i }
+ *     s_ij        = (q_i . k_j) / sqrt(D)
+ *     lse_i       = ln sum_{j in visible(i)} exp(s_ij)
+ *     out_i       = sum_{j in visible(i)} exp(s_ij - lse_i) v_j
+ * and the backward pass returns dq, dk, dv of L = sum(dout * out). The softmax scale
+ * is fixed at 1/sqrt(D). Rows whose segment id is negative (padding) see nothing:
+ * out = 0, lse = -inf, and they receive and contribute zero gradient.
+ *
+ * Layouts (all dense, row-major, device memory):
+ *   q, k, v, out, dout, dq, dk, dv : bf16  [B, S, H, D]  (D fastest)
+ *   lse                            : fp32  [B, H, S]     (natural log)
+ *   seg_ids, pos                   : int32 [B, S]
+ * Preconditions on seg_ids / pos, per batch row:
+ *   - documents are contiguous runs with non-decreasing ids >= 0, optionally followed
+ *     by one trailing run of negative ids (padding);
+ *   - pos[b, i] is the offset of token i inside its document (0, 1, 2, ... restarting
+ *     at each document). Position entries of padding tokens are ignored.
+ *   seg_ids == NULL means one document per row; pos == NULL means pos is derived
+ *   from seg_ids. Violations are detected on the device and reported by
+ *   lwm_attn_check() as LWM_ERR_SEGMENTS; the outputs of such a call are undefined.
+ *
+ * Ownership and synchronisation. The caller owns every buffer, including the
+ * workspace (size from lwm_attn_workspace_size()). The library never allocates or
+ * frees device memory and never synchronises, except in lwm_attn_check(). Every
+ * call only enqueues work on `stream`; calls that share one workspace must be
+ * ordered (same stream, or synchronised by the caller).
+ *
+ * Errors. Host-side argument errors return a status and enqueue nothing. Device-side
+ * conditions (inconsistent seg/pos, an internal wait that timed out) set an error
+ * word in the workspace that lwm_attn_check() returns and clears.
+ *
+ * Supported: D == 128 only; all pointers 16-byte aligned; 1 <= S, B, H; B*S*H*D
+ * below 2^31 elements per tensor dimension product as TMA coordinates allow.
+ */
+#ifndef LWM_ATTN_H
+#define LWM_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* bfloat16 storage (the raw 16-bit pattern). */
+typedef uint16_t lwm_bf16;
+/* A CUDA stream; the same type as cudaStream_t (NULL = legacy default stream). */
+typedef struct CUstream_st *lwm_stream;
+
+typedef enum {
+  LWM_OK = 0,
+  LWM_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, too-small workspace */
+  LWM_ERR_UNSUPPORTED = 2,  /* D != 128, or no sm_100-family device */
+  LWM_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned */
+  LWM_ERR_SEGMENTS = 4,     /* device: seg_ids / pos break the preconditions above */
+  LWM_ERR_WORKSPACE = 5,    /* workspace not 256-byte aligned */
+  LWM_ERR_CUDA = 6,         /* a CUDA runtime or driver call failed */
+  LWM_ERR_TIMEOUT = 7       /* device: an internal pipeline wait exceeded its bound */
+} lwm_status;
+
+/* Bytes of device workspace needed for problems of this shape (0 on bad sizes).
+ * The workspace holds the per-token segment starts, per-tile ranges, the schedule's
+ * work lists and tickets, the error word and the backward row dots (fp32 [B,H,S]). */
+size_t lwm_attn_workspace_size(int B, int S, int H, int D);
+
+/* Metadata pre-pass alone: validates seg_ids/pos and writes segment starts, per-tile
+ * key/query ranges and longest-first work lists into `workspace`. The *_prepared
+ * calls below reuse it, so one prepare serves every layer that shares a packing.
+ * kv_chunks >= 1 sets the ring order of the forward pass (see lwm_attn_fwd_ring). */
+lwm_status lwm_attn_prepare(const int32_t *seg_ids, const int32_t *pos, int B, int S, int H, int D,
+                            int kv_chunks, void *workspace, size_t workspace_bytes, lwm_stream stream);
+
+/* Forward pass: metadata pre-pass, then the persistent tensor-core kernel.
+ * Writes out [B,S,H,D] bf16 and lse [B,H,S] fp32. */
+lwm_status lwm_attn_fwd(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
+                        const int32_t *seg_ids, const int32_t *pos, lwm_bf16 *out, float *lse,
+                        int B, int S, int H, int D, void *workspace, size_t workspace_bytes,
+                        lwm_stream stream);
+
+/* Forward pass with the key/value blocks visited in ring order: the sequence is cut
+ * into kv_chunks equal chunks (the blocks that the devices of a ring would hold,
+ * LWM deep-dive page, section "RingAttention 为什么必要"), and a query block in chunk
+ * r visits chunks r, r-1, ..., 0, all inside one launch on one GPU. The result equals
+ * lwm_attn_fwd's up to floating-point rounding order. */
+lwm_status lwm_attn_fwd_ring(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
+                             const int32_t *seg_ids, const int32_t *pos, lwm_bf16 *out, float *lse,
+                             int B, int S, int H, int D, int kv_chunks, void *workspace,
+                             size_t workspace_bytes, lwm_stream stream);
+
+/* Forward pass reusing the metadata of a previous lwm_attn_prepare (same B, S and
+ * segments) held in `workspace`. */
+lwm_status lwm_attn_fwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
+                                 lwm_bf16 *out, float *lse, int B, int S, int H, int D,
+                                 void *workspace, size_t workspace_bytes, lwm_stream stream);
+
+/* Backward pass: metadata pre-pass, the row-dot pre-pass delta_i = dout_i . out_i,
+ * then the dK/dV kernel and the dQ kernel. `out` and `lse` are the forward outputs.
+ * dq, dk, dv are fully overwritten (no accumulation into existing values). */
+lwm_status lwm_attn_bwd(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
+                        const lwm_bf16 *out, const lwm_bf16 *dout, const float *lse,
+                        const int32_t *seg_ids, const int32_t *pos,
+                        lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv,
+                        int B, int S, int H, int D, void *workspace, size_t workspace_bytes,
+                        lwm_stream stream);
+
+/* Backward pass reusing the metadata of a previous lwm_attn_prepare in `workspace`. */
+lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
+                                 const lwm_bf16 *out, const lwm_bf16 *dout, const float *lse,
+                                 lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv,
+                                 int B, int S, int H, int D, void *workspace, size_t workspace_bytes,
+                                 lwm_stream stream);
+
+/* Synchronises `stream`, then returns and clears the device error word held in
+ * `workspace` (LWM_OK, LWM_ERR_SEGMENTS or LWM_ERR_TIMEOUT), or LWM_ERR_CUDA if the
+ * stream reported a CUDA error. */
+lwm_status lwm_attn_check(void *workspace, lwm_stream stream);
+
+/* Static, human-readable name of a status code. */
+const char *lwm_status_string(lwm_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LWM_ATTN_H */

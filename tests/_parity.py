@@ -1,0 +1,39 @@
+"""Helpers shared by the GPU parity tests: tensor conversion and the error metrics.
+
+Tolerances (the workload statement's bar): forward max |out - o| <= 1e-2, mean
+|out - o| <= 1e-3, max |lse - lse*| <= 1e-3 (natural log); gradients: relative L2
+error <= 1e-2 per tensor.
+"""
+
+import numpy as np
+import torch
+
+OUT_MAX, OUT_MEAN, LSE_MAX, GRAD_REL = 1e-2, 1e-3, 1e-3, 1e-2
+
+
+def f64(t):
+    return t.detach().to("cpu", torch.float32).numpy().astype(np.float64)
+
+
+def fwd_errors(out, lse, ref_out, ref_lse):
+    """(max abs, mean abs, lse max abs) over rows whose reference lse is finite;
+    rows with -inf reference lse must come back as exactly -inf with zero output."""
+    out = np.asarray(out); ref_out = np.asarray(ref_out)
+    lse = np.asarray(lse); ref_lse = np.asarray(ref_lse)
+    d = np.abs(out - ref_out)
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isneginf(lse), ~fin), "empty rows must have lse = -inf"
+    lerr = float(np.max(np.abs(lse[fin] - ref_lse[fin]))) if fin.any() else 0.0
+    return float(d.max()), float(d.mean()), lerr
+
+
+def assert_fwd(out, lse, ref_out, ref_lse, what=""):
+    mx, mean, le = fwd_errors(out, lse, ref_out, ref_lse)
+    assert mx <= OUT_MAX and mean <= OUT_MEAN and le <= LSE_MAX, \
+        f"{what}: max {mx:.3e} mean {mean:.3e} lse {le:.3e}"
+    return mx, mean, le
+
+
+def rel_l2(g, ref):
+    g = np.asarray(g); ref = np.asarray(ref)
+    return float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-30))
