@@ -22,7 +22,7 @@ __all__ = [
     "LwmError", "library_path", "load_library",
     "lwm_attn_workspace_size", "lwm_attn_prepare", "lwm_attn_fwd", "lwm_attn_fwd_ring",
     "lwm_attn_fwd_prepared", "lwm_attn_bwd", "lwm_attn_bwd_prepared", "lwm_attn_check",
-    "lwm_status_string", "new_workspace", "forward", "backward",
+    "lwm_status_string", "lwm_last_error", "new_workspace", "forward", "backward",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -45,6 +45,7 @@ _SIGNATURES = {
     "lwm_attn_bwd_prepared": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
     "lwm_attn_check": (_I, [_P, _P]),
     "lwm_status_string": (ctypes.c_char_p, [_I]),
+    "lwm_last_error": (ctypes.c_char_p, []),
 }
 
 
@@ -84,8 +85,14 @@ def lwm_status_string(status: int) -> str:
         return STATUS_NAMES.get(int(status), f"status {status}")
 
 
+def lwm_last_error() -> str:
+    return load_library().lwm_last_error().decode()
+
+
 def _check(status: int, where: str):
     if status != 0:
+        if status == 6:
+            where = f"{where} [{lwm_last_error()}]"
         raise LwmError(status, where)
 
 

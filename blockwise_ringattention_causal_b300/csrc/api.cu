@@ -24,9 +24,24 @@ std::mutex g_mu;
 DeviceInfo g_dev[MAX_DEVICES];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+thread_local char g_last_error[512] = "";
+
+lwm_status fail(const char *what, const char *detail) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", what, detail);
+  return LWM_ERR_CUDA;
+}
+
+lwm_status cuda_check(cudaError_t e, const char *what) {
+  if (e == cudaSuccess) return LWM_OK;
+  cudaGetLastError();   // clear the sticky-free error so later calls start clean
+  return fail(what, cudaGetErrorString(e));
+}
+
+#define from_cuda(call) cuda_check((call), #call)
+
 lwm_status device_info(DeviceInfo &out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return LWM_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return fail("cudaGetDevice", "no device");
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceInfo &d = g_dev[dev];
   if (!d.known) {
@@ -34,7 +49,7 @@ lwm_status device_info(DeviceInfo &out) {
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return LWM_ERR_CUDA;
+      return fail("cudaDeviceGetAttribute", "failed");
     d.supported = (major == 10 && minor == 3);   // the kernels are built for sm_103a
     d.num_sms = sms;
     d.known = true;
@@ -45,7 +60,7 @@ lwm_status device_info(DeviceInfo &out) {
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
             cudaSuccess ||
         q != cudaDriverEntryPointSuccess || fn == nullptr)
-      return LWM_ERR_CUDA;
+      return fail("cudaGetDriverEntryPointByVersion", "cuTensorMapEncodeTiled not found");
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   out = d;
@@ -54,14 +69,25 @@ lwm_status device_info(DeviceInfo &out) {
 
 // [B, S, H, 128] bf16, loaded as boxes of 64 dims x 1 head x 128 rows x 1 batch row,
 // 128-byte swizzled (the K-major / MN-major canonical layout of the MMA operands).
-bool make_map(CUtensorMap *m, const void *ptr, int B, int S, int H) {
+CUresult make_map_raw(CUtensorMap *m, const void *ptr, int B, int S, int H) {
   cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(H), cuuint64_t(S), cuuint64_t(B)};
   cuuint64_t strides[3] = {cuuint64_t(HD) * 2, cuuint64_t(H) * HD * 2, cuuint64_t(S) * H * HD * 2};
   cuuint32_t box[4] = {64, 1, 128, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+bool make_map(CUtensorMap *m, const void *ptr, int B, int S, int H) {
+  const CUresult r = make_map_raw(m, ptr, B, S, H);
+  if (r != CUDA_SUCCESS) {
+    char buf[64];
+    std::snprintf(buf, sizeof(buf), "CUresult %d", int(r));
+    fail("cuTensorMapEncodeTiled", buf);
+    return false;
+  }
+  return true;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -84,7 +110,7 @@ lwm_status check_workspace(const void *ws, size_t bytes, int B, int S, int H) {
   return LWM_OK;
 }
 
-lwm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LWM_OK : LWM_ERR_CUDA; }
+
 
 #define LWM_TRY(x)                 \
   do {                             \
@@ -221,15 +247,17 @@ lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm
 
 lwm_status lwm_attn_check(void *workspace, lwm_stream stream) {
   if (!workspace) return LWM_ERR_INVALID_ARG;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return LWM_ERR_CUDA;
+  LWM_TRY(from_cuda(cudaStreamSynchronize(stream)));
   int word = 0;
   int *hdr = static_cast<int *>(workspace);
-  if (cudaMemcpy(&word, hdr + HDR_ERR, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LWM_ERR_CUDA;
-  if (word != 0 && cudaMemset(hdr + HDR_ERR, 0, sizeof(int)) != cudaSuccess) return LWM_ERR_CUDA;
+  LWM_TRY(from_cuda(cudaMemcpy(&word, hdr + HDR_ERR, sizeof(int), cudaMemcpyDeviceToHost)));
+  if (word != 0) LWM_TRY(from_cuda(cudaMemset(hdr + HDR_ERR, 0, sizeof(int))));
   if (word & ERRBIT_SEGMENTS) return LWM_ERR_SEGMENTS;
   if (word & ERRBIT_TIMEOUT) return LWM_ERR_TIMEOUT;
   return LWM_OK;
 }
+
+const char *lwm_last_error(void) { return g_last_error; }
 
 const char *lwm_status_string(lwm_status status) {
   switch (status) {

@@ -15,6 +15,7 @@
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer (and the scheduler ticket)
 //   warp  9    tcgen05 MMA issuer (and TMEM owner)
+//   warps 10-11 idle (they keep 3 warps per SM sub-partition)
 // TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P (bf16) is written
 // over the first 64 columns of its S. MMA order per key tile j:
 //   S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
@@ -25,7 +26,7 @@
 namespace lwm {
 namespace {
 
-constexpr int FWD_WARPS = 10;
+constexpr int FWD_WARPS = 12;   // 3 warps per SM sub-partition: 168 registers each
 constexpr int FWD_THREADS = FWD_WARPS * 32;
 constexpr int WARP_PRODUCER = 8;
 constexpr int WARP_MMA = 9;
@@ -407,7 +408,7 @@ __device__ bool bounded_wait_plain(uint64_t *bar, uint32_t parity) {
   return true;
 }
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(FWD_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -456,7 +457,7 @@ __global__ void __maxnreg__(200)
     __syncwarp();
   } else if (warp == WARP_MMA) {
     ok = mma_role(a, smem, bars, tmem, kv_chunk, lane);
-  } else {
+  } else if (warp < 8) {
     ok = softmax_role(a, bars, tmem, kv_chunk, warp >> 2, warp, lane);
   }
   if (!ok) {

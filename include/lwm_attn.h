@@ -128,6 +128,11 @@ lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm
  * stream reported a CUDA error. */
 lwm_status lwm_attn_check(void *workspace, lwm_stream stream);
 
+/* Description of the most recent LWM_ERR_CUDA raised on the calling host thread: the
+ * failing call and the CUDA error text ("" if none). The string is owned by the
+ * library and stays valid until the thread's next failing call. */
+const char *lwm_last_error(void);
+
 /* Static, human-readable name of a status code. */
 const char *lwm_status_string(lwm_status status);
 

@@ -3,6 +3,12 @@
 Tolerances (the workload statement's bar): forward max |out - o| <= 1e-2, mean
 |out - o| <= 1e-3, max |lse - lse*| <= 1e-3 (natural log); gradients: relative L2
 error <= 1e-2 per tensor.
+
+Synthetic edge cases outside the five named workloads (documents of a few tokens,
+where |o| reaches 2-4) use a per-element bound derived from the bf16 arithmetic
+instead of the flat 1e-2: the output is rounded to bf16 (up to 2^-9 |o|) and the
+probabilities enter the P.V product as bf16 (up to 2^-9 relative per weight, i.e. up
+to 2^-9 max|v - o| on o), so |out - o| <= 1e-2 + 2^-8 |o| elementwise.
 """
 
 import numpy as np
@@ -27,10 +33,15 @@ def fwd_errors(out, lse, ref_out, ref_lse):
     return float(d.max()), float(d.mean()), lerr
 
 
-def assert_fwd(out, lse, ref_out, ref_lse, what=""):
+def assert_fwd(out, lse, ref_out, ref_lse, what="", bf16_bound=False):
     mx, mean, le = fwd_errors(out, lse, ref_out, ref_lse)
-    assert mx <= OUT_MAX and mean <= OUT_MEAN and le <= LSE_MAX, \
-        f"{what}: max {mx:.3e} mean {mean:.3e} lse {le:.3e}"
+    if bf16_bound:
+        excess = np.abs(np.asarray(out) - ref_out) - (OUT_MAX + 2.0 ** -8 * np.abs(ref_out))
+        assert excess.max() <= 0 and mean <= OUT_MEAN and le <= LSE_MAX, \
+            f"{what}: max {mx:.3e} (bound exceeded by {excess.max():.3e}) mean {mean:.3e} lse {le:.3e}"
+    else:
+        assert mx <= OUT_MAX and mean <= OUT_MEAN and le <= LSE_MAX, \
+            f"{what}: max {mx:.3e} mean {mean:.3e} lse {le:.3e}"
     return mx, mean, le
 
 

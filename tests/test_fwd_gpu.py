@@ -44,7 +44,7 @@ def test_ragged_and_packed_shapes(cuda_device, S, lengths):
     x = I.make_inputs(w, cuda_device, with_dout=False)
     out, lse = run_fwd(x)
     ref_o, ref_l = full_ref(x)
-    assert_fwd(f64(out), f64(lse), ref_o, ref_l, f"S={S}")
+    assert_fwd(f64(out), f64(lse), ref_o, ref_l, f"S={S}", bf16_bound=True)
 
 
 def test_batch_rows_with_different_packings(cuda_device):
@@ -53,7 +53,7 @@ def test_batch_rows_with_different_packings(cuda_device):
     assert (x["seg"][2, 664:] == -1).all()
     out, lse = run_fwd(x)
     ref_o, ref_l = full_ref(x)
-    assert_fwd(f64(out), f64(lse), ref_o, ref_l, "B=3")
+    assert_fwd(f64(out), f64(lse), ref_o, ref_l, "B=3", bf16_bound=True)
     assert torch.all(out[2, 664:] == 0)
 
 
@@ -92,7 +92,7 @@ def test_large_scores_stay_finite(cuda_device):
     out, lse = run_fwd(x)
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
     ref_o, ref_l = full_ref(x)
-    assert_fwd(f64(out), f64(lse), ref_o, ref_l, "q x 30")
+    assert_fwd(f64(out), f64(lse), ref_o, ref_l, "q x 30", bf16_bound=True)
 
 
 def test_bad_segments_are_reported(cuda_device):
