@@ -42,7 +42,7 @@ enum HeaderWord {
 
 struct Workspace {
   size_t off_hdr, off_lo, off_kend, off_list_fwd, off_list_kv, off_list_q, off_delta, off_lse2, total;
-  int nT, nP;
+  int nT, nP, S_pad;   // S_pad = nT * BM: per-row stride of lo, delta and lse2
 
   __host__ __device__ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -50,16 +50,17 @@ struct Workspace {
     Workspace w;
     w.nT = (S + BM - 1) / BM;
     w.nP = (w.nT + 1) / 2;
+    w.S_pad = w.nT * BM;
     size_t o = 0;
     w.off_hdr = o;      o += align256(HDR_WORDS * 4);
-    w.off_lo = o;       o += align256(size_t(B) * S * 4);
+    w.off_lo = o;       o += align256(size_t(B) * w.S_pad * 4);
     w.off_kend = o;     o += align256(size_t(B) * w.nT * 4);
     w.off_list_fwd = o; o += align256(size_t(B) * w.nP * 4);
     w.off_list_kv = o;  o += align256(size_t(B) * w.nT * 4);
     w.off_list_q = o;   o += align256(size_t(B) * w.nT * 4);
     // backward row terms, fp32 [B, H, nT * BM] (rows padded to whole tiles)
-    w.off_delta = o;    o += align256(size_t(B) * H * w.nT * BM * 4);
-    w.off_lse2 = o;     o += align256(size_t(B) * H * w.nT * BM * 4);
+    w.off_delta = o;    o += align256(size_t(B) * H * w.S_pad * 4);
+    w.off_lse2 = o;     o += align256(size_t(B) * H * w.S_pad * 4);
     w.total = o;
     return w;
   }
@@ -146,6 +147,16 @@ __device__ __forceinline__ void tma_load_4d(const CUtensorMap *map, uint64_t *ba
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+// Plain (untiled) bulk copy global -> shared; both addresses 16-byte aligned and
+// `bytes` a multiple of 16. Completion is signalled on `bar` (tx bytes).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -264,7 +275,7 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 // ----------------------------------------------------------------------------- tile ranges
 // Inclusive range of key tiles that query tile [q0, q0+BM) of one batch row needs.
 // `lo_row[i]` is the first key visible to query i (its document start; i+1 for
-// padding). Documents are contiguous, so lo is non-decreasing and the range is
+// padding and for the rows S..S_pad-1 past the end). Documents are contiguous, so lo is non-decreasing and the range is
 // [lo[q0] / BN, last_row / BN]. Empty (first > last) when no row sees anything.
 struct TileRange {
   int first, last;

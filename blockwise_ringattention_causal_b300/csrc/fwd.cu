@@ -62,7 +62,7 @@ struct FwdArgs {
   int *hdr;
   __nv_bfloat16 *out;
   float *lse;
-  int B, S, H, nP, n_items;
+  int B, S, H, nP, n_items, S_pad;
   float scale_log2;   // log2(e) / sqrt(D)
 };
 
@@ -101,7 +101,7 @@ struct Ranges {
 };
 
 __device__ __forceinline__ Ranges item_ranges(const FwdArgs &a, const Item &I) {
-  const int *lr = a.lo + size_t(I.b) * a.S;
+  const int *lr = a.lo + size_t(I.b) * a.S_pad;
   Ranges R;
   R.r[0] = q_tile_kv_range(lr, a.S, (2 * I.pair) * BM);
   R.r[1] = q_tile_kv_range(lr, a.S, (2 * I.pair + 1) * BM);
@@ -286,7 +286,7 @@ __device__ bool softmax_role(const FwdArgs &a, FwdBars *bars, uint32_t tmem, int
     const TileRange my = R.r[t];
     const int q0 = (2 * I.pair + t) * BM;
     const int i = q0 + r;
-    const int *lr = a.lo + size_t(I.b) * a.S;
+    const int *lr = a.lo + size_t(I.b) * a.S_pad;
     const int lo_i = i < a.S ? lr[i] : i + 1;
     const int qb = min(q0 + BM, a.S) - 1;
     const int lo_qb = q0 < a.S ? lr[qb] : 0;
@@ -516,6 +516,7 @@ cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   a.S = p.S;
   a.H = p.H;
   a.nP = w.nP;
+  a.S_pad = w.S_pad;
   a.n_items = p.B * w.nP * p.H;
   a.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
   const int grid = a.n_items < p.num_sms ? a.n_items : p.num_sms;

@@ -46,7 +46,7 @@ __device__ int block_incl_max(int v, int *scratch /* 32 ints */) {
 // Pass 1: validate seg/pos and compute lo. With pos given, lo is local; without it,
 // lo is the prefix max of document starts, finished by pass 2 across blocks.
 __global__ void __launch_bounds__(META_THREADS) meta_lo_kernel(const int *__restrict__ seg,
-                                                               const int *__restrict__ pos, int S,
+                                                               const int *__restrict__ pos, int S, int S_pad,
                                                                int *__restrict__ lo, int *__restrict__ blk_last,
                                                                int *__restrict__ err) {
   __shared__ int scratch[32];
@@ -79,13 +79,14 @@ __global__ void __launch_bounds__(META_THREADS) meta_lo_kernel(const int *__rest
     my_lo = v;   // -1: the document started in an earlier block (pass 2)
     if (threadIdx.x == META_THREADS - 1) blk_last[size_t(b) * gridDim.x + blockIdx.x] = v;
   }
-  if (in) lo[row + i] = pad ? i + 1 : my_lo;
+  if (in) lo[size_t(b) * S_pad + i] = pad ? i + 1 : my_lo;
+  else if (i < S_pad) lo[size_t(b) * S_pad + i] = i + 1;   // rows past the end see nothing
   if (bad) raise_error(err, ERRBIT_SEGMENTS);
 }
 
 // Pass 2 (pos == NULL only): carry the last document start of earlier blocks.
 __global__ void __launch_bounds__(META_THREADS) meta_lo_carry_kernel(const int *__restrict__ seg, int S,
-                                                                     int *__restrict__ lo,
+                                                                     int S_pad, int *__restrict__ lo,
                                                                      const int *__restrict__ blk_last) {
   __shared__ int red[32];
   const int b = blockIdx.y;
@@ -99,20 +100,21 @@ __global__ void __launch_bounds__(META_THREADS) meta_lo_carry_kernel(const int *
   for (int k = 1; k < 32; ++k) carry = max(carry, red[k]);
   const int i = blockIdx.x * META_THREADS + threadIdx.x;
   if (i < S) {
-    const size_t idx = size_t(b) * S + i;
-    const int si = seg ? seg[idx] : 0;
-    if (si >= 0 && lo[idx] < 0) lo[idx] = carry;
+    const int si = seg ? seg[size_t(b) * S + i] : 0;
+    int &l = lo[size_t(b) * S_pad + i];
+    if (si >= 0 && l < 0) l = carry;
   }
 }
 
 // Per key tile: end (exclusive) of the query rows that see any of its keys. The rows
 // that see key tile [k0, k1) are i >= k0 with lo[i] <= k1 - 1; lo is non-decreasing,
 // so they form [k0, kend) with kend the first i >= k0 with lo[i] >= k1.
-__global__ void meta_kend_kernel(const int *__restrict__ lo, int B, int S, int nT, int *__restrict__ kend) {
+__global__ void meta_kend_kernel(const int *__restrict__ lo, int B, int S, int S_pad, int nT,
+                                 int *__restrict__ kend) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= B * nT) return;
   const int b = t / nT, kt = t % nT;
-  const int *lr = lo + size_t(b) * S;
+  const int *lr = lo + size_t(b) * S_pad;
   const int k0 = kt * BN, k1 = min(k0 + BN, S);
   int a = k0, z = S;   // first index in [a, z) with lr[idx] >= k1
   while (a < z) {
@@ -137,7 +139,7 @@ __device__ __forceinline__ int range_size(const int *lr, int S, int q0) {
 // Items of equal cost keep no particular order. The block also resets the tickets.
 __global__ void __launch_bounds__(META_THREADS) meta_sort_kernel(const int *__restrict__ lo,
                                                                  const int *__restrict__ kend, int B, int S,
-                                                                 int nT, int nP, int *__restrict__ hdr,
+                                                                 int S_pad, int nT, int nP, int *__restrict__ hdr,
                                                                  int *__restrict__ list_fwd,
                                                                  int *__restrict__ list_kv,
                                                                  int *__restrict__ list_q, int kv_chunk) {
@@ -157,14 +159,14 @@ __global__ void __launch_bounds__(META_THREADS) meta_sort_kernel(const int *__re
   auto cost_of = [&](int idx) -> int {
     if (which == 0) {
       const int b = idx / nP, p = idx % nP;
-      const int *lr = lo + size_t(b) * S;
+      const int *lr = lo + size_t(b) * S_pad;
       return range_size(lr, S, (2 * p) * BM) + range_size(lr, S, (2 * p + 1) * BM);
     } else if (which == 1) {
       const int b = idx / nT, kt = idx % nT;
       const int k0 = kt * BN, e = kend[idx];
       return e > k0 ? (e - 1) / BM - k0 / BM + 1 : 0;
     } else {
-      return range_size(lo + size_t(idx / nT) * S, S, (idx % nT) * BM);
+      return range_size(lo + size_t(idx / nT) * S_pad, S, (idx % nT) * BM);
     }
   };
   // bins in descending cost order: bin 0 holds the largest costs
@@ -231,12 +233,13 @@ cudaError_t launch_meta(const int *seg, const int *pos, int B, int S, int kv_chu
   // per-block carries of pass 1
   int *blk_last = reinterpret_cast<int *>(base + w.off_delta);
 
-  const dim3 g1((S + META_THREADS - 1) / META_THREADS, B);
-  meta_lo_kernel<<<g1, META_THREADS, 0, stream>>>(seg, pos, S, lo, blk_last, hdr + HDR_ERR);
-  if (!pos) meta_lo_carry_kernel<<<g1, META_THREADS, 0, stream>>>(seg, S, lo, blk_last);
+  const dim3 g1((w.S_pad + META_THREADS - 1) / META_THREADS, B);
+  meta_lo_kernel<<<g1, META_THREADS, 0, stream>>>(seg, pos, S, w.S_pad, lo, blk_last, hdr + HDR_ERR);
+  if (!pos) meta_lo_carry_kernel<<<g1, META_THREADS, 0, stream>>>(seg, S, w.S_pad, lo, blk_last);
   const int nk = B * w.nT;
-  meta_kend_kernel<<<(nk + 255) / 256, 256, 0, stream>>>(lo, B, S, w.nT, kend);
-  meta_sort_kernel<<<3, META_THREADS, 0, stream>>>(lo, kend, B, S, w.nT, w.nP, hdr, lf, lk, lq, kv_chunk);
+  meta_kend_kernel<<<(nk + 255) / 256, 256, 0, stream>>>(lo, B, S, w.S_pad, w.nT, kend);
+  meta_sort_kernel<<<3, META_THREADS, 0, stream>>>(lo, kend, B, S, w.S_pad, w.nT, w.nP, hdr, lf, lk, lq,
+                                                   kv_chunk);
   return cudaGetLastError();
 }
 
