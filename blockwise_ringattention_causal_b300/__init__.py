@@ -21,7 +21,8 @@ import torch
 __all__ = [
     "LwmError", "library_path", "load_library",
     "lwm_attn_workspace_size", "lwm_attn_prepare", "lwm_attn_fwd", "lwm_attn_fwd_ring",
-    "lwm_attn_fwd_prepared", "lwm_attn_bwd", "lwm_attn_bwd_prepared", "lwm_attn_check",
+    "lwm_attn_fwd_prepared", "lwm_attn_bwd", "lwm_attn_bwd_prepared", "lwm_attn_bwd_stages",
+    "lwm_attn_check",
     "lwm_status_string", "lwm_last_error", "new_workspace", "forward", "backward",
 ]
 
@@ -43,6 +44,7 @@ _SIGNATURES = {
     "lwm_attn_fwd_prepared": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
     "lwm_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
     "lwm_attn_bwd_prepared": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
+    "lwm_attn_bwd_stages": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_uint, _P, _Z, _P]),
     "lwm_attn_check": (_I, [_P, _P]),
     "lwm_status_string": (ctypes.c_char_p, [_I]),
     "lwm_last_error": (ctypes.c_char_p, []),
@@ -203,6 +205,24 @@ def lwm_attn_bwd_prepared(q, k, v, out, dout, lse, dq, dk, dv, workspace, stream
     _check(load_library().lwm_attn_bwd_prepared(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
                                                 _ptr(dq), _ptr(dk), _ptr(dv), B, S, H, D, _ptr(workspace),
                                                 workspace.numel(), _stream(stream)), "lwm_attn_bwd_prepared")
+
+
+LWM_BWD_DELTA, LWM_BWD_DKDV, LWM_BWD_DQ, LWM_BWD_ALL = 1, 2, 4, 7
+
+
+def lwm_attn_bwd_stages(q, k, v, out, dout, lse, dq, dk, dv, stages, workspace, stream=None):
+    """Selected backward stages (bit mask of LWM_BWD_*); unused tensors may be None."""
+    B, S, H, D = _shape(q if q is not None else out)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"), (dk, "dk"),
+                 (dv, "dv")):
+        if t is not None:
+            _need(t, n, torch.bfloat16, (B, S, H, D))
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, S))
+    _check(load_library().lwm_attn_bwd_stages(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                              _ptr(dq), _ptr(dk), _ptr(dv), B, S, H, D, int(stages),
+                                              _ptr(workspace), workspace.numel(), _stream(stream)),
+           "lwm_attn_bwd_stages")
 
 
 def lwm_attn_check(workspace, stream=None) -> int:

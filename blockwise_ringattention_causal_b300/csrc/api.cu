@@ -162,15 +162,49 @@ lwm_status check_bwd_args(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *
 
 lwm_status bwd_common(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,
                       const lwm_bf16 *dout, const float *lse, lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv, int B,
-                      int S, int H, void *ws, cudaStream_t stream, const DeviceInfo &d) {
+                      int S, int H, unsigned stages, void *ws, cudaStream_t stream, const DeviceInfo &d) {
+  Problem p{B, S, H, d.num_sms};
+  if (stages & LWM_BWD_DELTA) LWM_TRY(from_cuda(launch_delta(out, dout, lse, p, ws, stream)));
+  if (!(stages & (LWM_BWD_DKDV | LWM_BWD_DQ))) return LWM_OK;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_map(&tq, q, B, S, H) || !make_map(&tk, k, B, S, H) || !make_map(&tv, v, B, S, H) ||
       !make_map(&tdo, dout, B, S, H))
     return LWM_ERR_CUDA;
-  Problem p{B, S, H, d.num_sms};
-  LWM_TRY(from_cuda(launch_delta(out, dout, lse, p, ws, stream)));
-  LWM_TRY(from_cuda(launch_dkdv(tq, tk, tv, tdo, dk, dv, p, ws, stream)));
-  return from_cuda(launch_dq(tq, tk, tv, tdo, dq, p, ws, stream));
+  if (stages & LWM_BWD_DKDV) LWM_TRY(from_cuda(launch_dkdv(tq, tk, tv, tdo, dk, dv, p, ws, stream)));
+  if (stages & LWM_BWD_DQ) LWM_TRY(from_cuda(launch_dq(tq, tk, tv, tdo, dq, p, ws, stream)));
+  return LWM_OK;
+}
+
+// Argument checks for the selected backward stages only.
+lwm_status check_stage_args(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,
+                            const lwm_bf16 *dout, const float *lse, lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv,
+                            int B, int S, int H, int D, unsigned stages, void *ws, size_t ws_bytes) {
+  LWM_TRY(check_sizes(B, S, H, D));
+  if (stages == 0 || (stages & ~unsigned(LWM_BWD_ALL))) return LWM_ERR_INVALID_ARG;
+  const void *need16[8];
+  int n = 0;
+  if (stages & LWM_BWD_DELTA) {
+    if (!lse) return LWM_ERR_INVALID_ARG;
+    if (!aligned4(lse)) return LWM_ERR_ALIGNMENT;
+    need16[n++] = out;
+    need16[n++] = dout;
+  }
+  if (stages & (LWM_BWD_DKDV | LWM_BWD_DQ)) {
+    need16[n++] = q;
+    need16[n++] = k;
+    need16[n++] = v;
+    need16[n++] = dout;
+  }
+  if (stages & LWM_BWD_DKDV) {
+    need16[n++] = dk;
+    need16[n++] = dv;
+  }
+  if (stages & LWM_BWD_DQ) need16[n++] = dq;
+  for (int i = 0; i < n; ++i) {
+    if (!need16[i]) return LWM_ERR_INVALID_ARG;
+    if (!aligned16(need16[i])) return LWM_ERR_ALIGNMENT;
+  }
+  return check_workspace(ws, ws_bytes, B, S, H);
 }
 
 }  // namespace
@@ -232,7 +266,7 @@ lwm_status lwm_attn_bwd(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
   DeviceInfo d;
   LWM_TRY(device_info(d));
   LWM_TRY(prepare_impl(seg_ids, pos, B, S, H, 1, workspace, stream));
-  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, workspace, stream, d);
+  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, LWM_BWD_ALL, workspace, stream, d);
 }
 
 lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,
@@ -242,7 +276,17 @@ lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm
   LWM_TRY(check_bwd_args(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, D, workspace, workspace_bytes));
   DeviceInfo d;
   LWM_TRY(device_info(d));
-  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, workspace, stream, d);
+  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, LWM_BWD_ALL, workspace, stream, d);
+}
+
+lwm_status lwm_attn_bwd_stages(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,
+                               const lwm_bf16 *dout, const float *lse, lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv,
+                               int B, int S, int H, int D, unsigned stages, void *workspace,
+                               size_t workspace_bytes, lwm_stream stream) {
+  LWM_TRY(check_stage_args(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, D, stages, workspace, workspace_bytes));
+  DeviceInfo d;
+  LWM_TRY(device_info(d));
+  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, stages, workspace, stream, d);
 }
 
 lwm_status lwm_attn_check(void *workspace, lwm_stream stream) {

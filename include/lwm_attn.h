@@ -123,6 +123,26 @@ lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm
                                  int B, int S, int H, int D, void *workspace, size_t workspace_bytes,
                                  lwm_stream stream);
 
+/* Stages of the backward pass, for lwm_attn_bwd_stages (a bit mask). */
+typedef enum {
+  LWM_BWD_DELTA = 1,  /* row dots delta = rowsum(dout * out) and lse rows, into the workspace */
+  LWM_BWD_DKDV = 2,   /* dk, dv (needs LWM_BWD_DELTA's results in the workspace) */
+  LWM_BWD_DQ = 4,     /* dq (needs LWM_BWD_DELTA's results in the workspace) */
+  LWM_BWD_ALL = 7
+} lwm_bwd_stage;
+
+/* Runs the selected backward stages in the order delta, dK/dV, dQ, reusing the
+ * metadata of a previous lwm_attn_prepare. After the delta stage has completed, the
+ * dK/dV and dQ stages only read the workspace (each has its own scheduler ticket), so
+ * a caller may run them on two streams. Pointers that no selected stage touches may
+ * be NULL (delta: out, dout, lse; dK/dV: q, k, v, dout, dk, dv; dQ: q, k, v, dout,
+ * dq). lwm_attn_bwd_prepared is stages = LWM_BWD_ALL. */
+lwm_status lwm_attn_bwd_stages(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
+                               const lwm_bf16 *out, const lwm_bf16 *dout, const float *lse,
+                               lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv,
+                               int B, int S, int H, int D, unsigned stages, void *workspace,
+                               size_t workspace_bytes, lwm_stream stream);
+
 /* Synchronises `stream`, then returns and clears the device error word held in
  * `workspace` (LWM_OK, LWM_ERR_SEGMENTS or LWM_ERR_TIMEOUT), or LWM_ERR_CUDA if the
  * stream reported a CUDA error. */
