@@ -48,6 +48,7 @@ _SIGNATURES = {
     "lwm_attn_check": (_I, [_P, _P]),
     "lwm_status_string": (ctypes.c_char_p, [_I]),
     "lwm_last_error": (ctypes.c_char_p, []),
+    "lwm_attn_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
 }
 
 

@@ -208,6 +208,19 @@ lwm_status check_stage_args(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16
 }
 
 }  // namespace
+
+// Forward pass (metadata pre-pass + forward kernel) into a workspace that holds at
+// least the forward part of the layout (Workspace::layout(B, S, 1).total bytes).
+// Arguments are checked by the caller.
+lwm_status fwd_with_forward_workspace(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const int32_t *seg,
+                                      const int32_t *pos, lwm_bf16 *out, float *lse, int B, int S, int H, void *ws,
+                                      cudaStream_t stream) {
+  DeviceInfo d;
+  LWM_TRY(device_info(d));
+  LWM_TRY(prepare_impl(seg, pos, B, S, H, 1, ws, stream));
+  return fwd_common(q, k, v, out, lse, B, S, H, ws, stream, d);
+}
+
 }  // namespace lwm
 
 using namespace lwm;

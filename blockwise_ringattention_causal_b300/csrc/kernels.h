@@ -29,3 +29,13 @@ cudaError_t launch_dq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtens
                       cudaStream_t stream);
 
 }  // namespace lwm
+
+#include "lwm_attn.h"
+
+namespace lwm {
+
+lwm_status fwd_with_forward_workspace(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const int32_t *seg,
+                                      const int32_t *pos, lwm_bf16 *out, float *lse, int B, int S, int H, void *ws,
+                                      cudaStream_t stream);
+
+}  // namespace lwm

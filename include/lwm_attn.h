@@ -143,6 +143,38 @@ lwm_status lwm_attn_bwd_stages(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_b
                                int B, int S, int H, int D, unsigned stages, void *workspace,
                                size_t workspace_bytes, lwm_stream stream);
 
+/* Bytes of the library's own device scratch array used by lwm_attn_fwd_noalloc. */
+#define LWM_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* Forward pass for callers that cannot allocate device memory. This entry point has
+ * no counterpart in the LWM pages; it exists for callers with no way to obtain a
+ * workspace: a plug-in inside a host framework that owns all device memory and hands
+ * its plug-ins only their tensors, or a latency-critical caller that must not call
+ * cudaMalloc because cudaMalloc may synchronise the whole device.
+ *
+ * It computes exactly what lwm_attn_fwd computes (same kernels), with the workspace
+ * replaced by a 16 MiB device array (LWM_NOALLOC_SCRATCH_BYTES) that the library
+ * declares at file scope: every GPU on which the library is loaded holds that array
+ * until the process exits. The caller still passes inputs and outputs. Nothing is
+ * allocated or freed: no cudaMalloc, cudaFree or allocating library routine.
+ *   - Limit: the forward part of the workspace for (B, S) must fit the array, which
+ *     holds about 12 bytes per token: B * S up to about 1.3 million tokens (S rounded
+ *     up per row to a multiple of 128). Larger problems return LWM_ERR_INVALID_ARG
+ *     before anything is enqueued.
+ *   - Set-up: the first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (with that device current) and caches it; make that first
+ *     call before any stream capture.
+ *   - Sharing: all calls on a device share the one array and it keeps the last call's
+ *     contents; each call clears the words that must start at zero. Calls that overlap
+ *     on the GPU (different streams, or several host threads) race on the array and
+ *     must be serialised by the caller.
+ *   - Errors: argument errors are returned as by lwm_attn_fwd. Device-side conditions
+ *     (seg_ids / pos that break the preconditions) are not reported, because the error
+ *     word lives in the shared array; the outputs for such inputs are undefined. */
+lwm_status lwm_attn_fwd_noalloc(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
+                                const int32_t *seg_ids, const int32_t *pos, lwm_bf16 *out, float *lse,
+                                int B, int S, int H, int D, lwm_stream stream);
+
 /* Synchronises `stream`, then returns and clears the device error word held in
  * `workspace` (LWM_OK, LWM_ERR_SEGMENTS or LWM_ERR_TIMEOUT), or LWM_ERR_CUDA if the
  * stream reported a CUDA error. */
