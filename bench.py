@@ -162,8 +162,7 @@ def run_reference(args, rank):
     """--impl reference: the float64 oracle on the host cores, a bounded sample per step."""
     if rank != 0:
         return
-    from blockwise_ringattention_causal_b300 import inputs as I
-    w = I.workload(args.config)
+    w = workload_of(args)
     S_sample = 8192
     for _ in range(args.warmup):
         oracle_sample(S_sample, 1)
@@ -186,13 +185,21 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def workload_of(args):
+    from blockwise_ringattention_causal_b300 import inputs as I
+    if args.seq > 0:
+        return I.custom(args.batch, args.seq, args.heads, 128, None, seed=0,
+                        name=f"causal-S{args.seq}-H{args.heads}-B{args.batch}")
+    return I.workload(args.config)
+
+
 # ----------------------------------------------------------------------------- GPU leg
 def run_ours(args, rank, world):
     import blockwise_ringattention_causal_b300 as lwm
     from blockwise_ringattention_causal_b300 import inputs as I
 
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = I.workload(args.config)
+    w = workload_of(args)
     B, S, H, D = w.B, w.S, w.H, w.D
     x = I.make_inputs(w, dev, with_dout=w.backward)
     q, k, v, seg, pos = x["q"], x["k"], x["v"], x["seg"], x["pos"]
@@ -357,6 +364,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=2, help="1..5 (2 = S=32K, H=32, D=128 causal)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seq", type=int, default=0, help="custom workload: sequence length (one document)")
+    ap.add_argument("--heads", type=int, default=32, help="custom workload: heads")
+    ap.add_argument("--batch", type=int, default=1, help="custom workload: batch rows")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
