@@ -147,6 +147,7 @@ def oracle_sample(S_sample, heads, seed=0):
         threads = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
     except ImportError:
         threads = 1
+    threads = min(threads, len(os.sched_getaffinity(0)))
     g = torch.Generator().manual_seed(seed)
     q, k, v, do = (torch.randn((1, S_sample, heads, 128), generator=g).to(torch.bfloat16).float().numpy()
                    for _ in range(4))
@@ -215,7 +216,9 @@ def run_ours(args, rank, world):
     flops_step = (14.0 if w.backward else 4.0) * D * H * pairs
 
     # kernel name -> (events before, after) inside each timed step
-    names = ["meta", "fwd"] + (["delta", "dkdv", "dq"] if w.backward else [])
+    fused = args.bwd == "fused"
+    bwd_names = ["delta", "dkdvq"] if fused else ["delta", "dkdv", "dq"]
+    names = ["meta", "fwd"] + (bwd_names if w.backward else [])
 
     def step(ev=None):
         def mark(i):
@@ -229,12 +232,18 @@ def run_ours(args, rank, world):
         if w.backward:
             lwm.lwm_attn_bwd_stages(None, None, None, out, dout, lse, None, None, None, lwm.LWM_BWD_DELTA, ws, stream)
             mark(3)
-            lwm.lwm_attn_bwd_stages(q, k, v, None, dout, None, None, dk, dv, lwm.LWM_BWD_DKDV, ws, stream)
-            mark(4)
-            lwm.lwm_attn_bwd_stages(q, k, v, None, dout, None, dq, None, None, lwm.LWM_BWD_DQ, ws, stream)
-            mark(5)
+            if fused:
+                # memset of the dQ accumulator, the single backward kernel, dq conversion
+                lwm.lwm_attn_bwd_stages(q, k, v, None, dout, None, dq, dk, dv, lwm.LWM_BWD_FUSED, ws, stream)
+                mark(4)
+            else:
+                lwm.lwm_attn_bwd_stages(q, k, v, None, dout, None, None, dk, dv, lwm.LWM_BWD_DKDV, ws, stream)
+                mark(4)
+                lwm.lwm_attn_bwd_stages(q, k, v, None, dout, None, dq, None, None, lwm.LWM_BWD_DQ, ws, stream)
+                mark(5)
 
-    launches_per_step = 3 + 1 + (3 if w.backward else 0)   # meta (3 kernels), fwd, delta, dK/dV, dQ
+    # meta (3 kernels), fwd, then delta + (dK/dV/dQ kernel + dq conversion | dK/dV + dQ)
+    launches_per_step = 3 + 1 + (3 if w.backward else 0)
 
     for _ in range(args.warmup):
         step()
@@ -273,7 +282,8 @@ def run_ours(args, rank, world):
     fwd_tflops = flops_fwd / (per_kernel["fwd"] * 1e-3) / 1e12
 
     # roofline of the dominant kernel (largest share of the step)
-    alg = {"fwd": 4.0 * D * H * pairs, "dkdv": 8.0 * D * H * pairs, "dq": 6.0 * D * H * pairs}
+    alg = {"fwd": 4.0 * D * H * pairs, "dkdv": 8.0 * D * H * pairs, "dq": 6.0 * D * H * pairs,
+           "dkdvq": 10.0 * D * H * pairs}
     dom = max((n for n in alg if n in per_kernel), key=lambda n: per_kernel[n])
     peaks = load_peaks()
     achieved = alg[dom] / (per_kernel[dom] * 1e-3) / 1e12
@@ -333,11 +343,12 @@ def run_ours(args, rank, world):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        S_sample, heads = 8192, 2
+        S_sample, heads = 8192, 6
         dt, fl, threads = oracle_sample(S_sample, heads)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"float64 oracle forward+backward of {heads} heads x first {S_sample} tokens of one "
-                         f"causal document (D=128), {dt:.1f} s"}
+                         f"causal document (D=128), {dt:.1f} s; BLAS threads {threads} of "
+                         f"{len(os.sched_getaffinity(0))} host CPUs"}
 
     if rank == 0:
         line = {
@@ -367,6 +378,8 @@ def main():
     ap.add_argument("--seq", type=int, default=0, help="custom workload: sequence length (one document)")
     ap.add_argument("--heads", type=int, default=32, help="custom workload: heads")
     ap.add_argument("--batch", type=int, default=1, help="custom workload: batch rows")
+    ap.add_argument("--bwd", choices=["fused", "separate"], default="fused",
+                    help="backward path: one dK/dV/dQ kernel (default) or separate dK/dV and dQ kernels")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

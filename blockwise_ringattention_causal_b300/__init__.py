@@ -20,7 +20,7 @@ import torch
 
 __all__ = [
     "LwmError", "library_path", "load_library",
-    "lwm_attn_workspace_size", "lwm_attn_prepare", "lwm_attn_fwd", "lwm_attn_fwd_ring",
+    "lwm_attn_workspace_size", "lwm_attn_workspace_size_fwd", "lwm_attn_prepare", "lwm_attn_fwd", "lwm_attn_fwd_ring",
     "lwm_attn_fwd_prepared", "lwm_attn_bwd", "lwm_attn_bwd_prepared", "lwm_attn_bwd_stages",
     "lwm_attn_check",
     "lwm_status_string", "lwm_last_error", "new_workspace", "forward", "backward",
@@ -38,6 +38,7 @@ STATUS_NAMES = {
 _P, _I, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 _SIGNATURES = {
     "lwm_attn_workspace_size": (_Z, [_I, _I, _I, _I]),
+    "lwm_attn_workspace_size_fwd": (_Z, [_I, _I, _I, _I]),
     "lwm_attn_prepare": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "lwm_attn_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
     "lwm_attn_fwd_ring": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
@@ -138,9 +139,14 @@ def lwm_attn_workspace_size(B, S, H, D) -> int:
     return int(load_library().lwm_attn_workspace_size(B, S, H, D))
 
 
-def new_workspace(B, S, H, D, device="cuda") -> torch.Tensor:
-    """A zero-filled workspace (the library requires zeros before first use)."""
-    n = lwm_attn_workspace_size(B, S, H, D)
+def lwm_attn_workspace_size_fwd(B, S, H, D) -> int:
+    return int(load_library().lwm_attn_workspace_size_fwd(B, S, H, D))
+
+
+def new_workspace(B, S, H, D, device="cuda", forward_only=False) -> torch.Tensor:
+    """A zero-filled workspace (the library requires zeros before first use).
+    ``forward_only`` leaves out the dQ accumulator that only the backward pass uses."""
+    n = (lwm_attn_workspace_size_fwd if forward_only else lwm_attn_workspace_size)(B, S, H, D)
     if n == 0:
         raise ValueError("unsupported sizes")
     return torch.zeros(n, dtype=torch.uint8, device=device)
@@ -208,7 +214,7 @@ def lwm_attn_bwd_prepared(q, k, v, out, dout, lse, dq, dk, dv, workspace, stream
                                                 workspace.numel(), _stream(stream)), "lwm_attn_bwd_prepared")
 
 
-LWM_BWD_DELTA, LWM_BWD_DKDV, LWM_BWD_DQ, LWM_BWD_ALL = 1, 2, 4, 7
+LWM_BWD_DELTA, LWM_BWD_DKDV, LWM_BWD_DQ, LWM_BWD_ALL, LWM_BWD_FUSED = 1, 2, 4, 7, 8
 
 
 def lwm_attn_bwd_stages(q, k, v, out, dout, lse, dq, dk, dv, stages, workspace, stream=None):
@@ -245,11 +251,20 @@ def forward(q, k, v, seg_ids=None, pos=None, kv_chunks=1, workspace=None, stream
     return out, lse, workspace
 
 
-def backward(q, k, v, out, dout, lse, seg_ids=None, pos=None, workspace=None, stream=None):
-    """Allocate dq/dk/dv and run the backward pass. Returns (dq, dk, dv)."""
+def backward(q, k, v, out, dout, lse, seg_ids=None, pos=None, workspace=None, stream=None, deterministic=False):
+    """Allocate dq/dk/dv and run the backward pass. Returns (dq, dk, dv).
+
+    The default runs lwm_attn_bwd (row-dot pre-pass + single-kernel dK/dV/dQ, dq summed
+    in fp32 in a scheduling-dependent order). ``deterministic=True`` runs the
+    metadata pre-pass and the LWM_BWD_ALL stages (separate dK/dV and dQ kernels,
+    every gradient bitwise reproducible)."""
     B, S, H, D = _shape(q)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
         workspace = new_workspace(B, S, H, D, q.device)
-    lwm_attn_bwd(q, k, v, out, dout, lse, seg_ids, pos, dq, dk, dv, workspace, stream)
+    if deterministic:
+        lwm_attn_prepare(seg_ids, pos, B, S, H, D, 1, workspace, stream)
+        lwm_attn_bwd_stages(q, k, v, out, dout, lse, dq, dk, dv, LWM_BWD_ALL, workspace, stream)
+    else:
+        lwm_attn_bwd(q, k, v, out, dout, lse, seg_ids, pos, dq, dk, dv, workspace, stream)
     return dq, dk, dv

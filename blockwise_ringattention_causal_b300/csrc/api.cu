@@ -67,24 +67,44 @@ lwm_status device_info(DeviceInfo &out) {
   return d.supported ? LWM_OK : LWM_ERR_UNSUPPORTED;
 }
 
-// [B, S, H, 128] bf16, loaded as boxes of 64 dims x 1 head x 128 rows x 1 batch row,
+// [B, S, H, 128] bf16, loaded as boxes of 64 dims x 1 head x `rows` rows x 1 batch row,
 // 128-byte swizzled (the K-major / MN-major canonical layout of the MMA operands).
-CUresult make_map_raw(CUtensorMap *m, const void *ptr, int B, int S, int H) {
+CUresult make_map_raw(CUtensorMap *m, const void *ptr, int B, int S, int H, int rows) {
   cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(H), cuuint64_t(S), cuuint64_t(B)};
   cuuint64_t strides[3] = {cuuint64_t(HD) * 2, cuuint64_t(H) * HD * 2, cuuint64_t(S) * H * HD * 2};
-  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t box[4] = {64, 1, cuuint32_t(rows), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-bool make_map(CUtensorMap *m, const void *ptr, int B, int S, int H) {
-  const CUresult r = make_map_raw(m, ptr, B, S, H);
+bool make_map(CUtensorMap *m, const void *ptr, int B, int S, int H, int rows = BM) {
+  const CUresult r = make_map_raw(m, ptr, B, S, H, rows);
   if (r != CUDA_SUCCESS) {
     char buf[64];
     std::snprintf(buf, sizeof(buf), "CUresult %d", int(r));
     fail("cuTensorMapEncodeTiled", buf);
+    return false;
+  }
+  return true;
+}
+
+// The fp32 dQ accumulator [B * H * S_pad rows, 128 dims] of the workspace, written by
+// tensor reduce-add copies of 16-row x 32-dim boxes.
+bool make_dqacc_map(CUtensorMap *m, void *ws, int B, int S, int H) {
+  const Workspace w = Workspace::layout(B, S, H);
+  cuuint64_t dims[2] = {cuuint64_t(HD), cuuint64_t(B) * H * w.S_pad};
+  cuuint64_t strides[1] = {cuuint64_t(HD) * 4};
+  cuuint32_t box[2] = {32, 16};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, static_cast<char *>(ws) + w.off_dqacc, dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[64];
+    std::snprintf(buf, sizeof(buf), "CUresult %d", int(r));
+    fail("cuTensorMapEncodeTiled (dQ accumulator)", buf);
     return false;
   }
   return true;
@@ -103,10 +123,13 @@ lwm_status check_sizes(int B, int S, int H, int D) {
   return LWM_OK;
 }
 
-lwm_status check_workspace(const void *ws, size_t bytes, int B, int S, int H) {
+// `with_dqacc`: the call runs the single-kernel backward pass, which needs the whole
+// layout; every other call needs only the part in front of the dQ accumulator.
+lwm_status check_workspace(const void *ws, size_t bytes, int B, int S, int H, bool with_dqacc) {
   if (!ws) return LWM_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LWM_ERR_WORKSPACE;
-  if (bytes < Workspace::layout(B, S, H).total) return LWM_ERR_INVALID_ARG;
+  const Workspace w = Workspace::layout(B, S, H);
+  if (bytes < (with_dqacc ? w.total : w.off_dqacc)) return LWM_ERR_INVALID_ARG;
   return LWM_OK;
 }
 
@@ -141,7 +164,7 @@ lwm_status check_fwd_args(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *
   if (!q || !k || !v || !out || !lse) return LWM_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned4(lse))
     return LWM_ERR_ALIGNMENT;
-  return check_workspace(ws, ws_bytes, B, S, H);
+  return check_workspace(ws, ws_bytes, B, S, H, false);
 }
 
 lwm_status check_seg_args(const int32_t *seg, const int32_t *pos) {
@@ -157,7 +180,7 @@ lwm_status check_bwd_args(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse))
     return LWM_ERR_ALIGNMENT;
-  return check_workspace(ws, ws_bytes, B, S, H);
+  return check_workspace(ws, ws_bytes, B, S, H, true);
 }
 
 lwm_status bwd_common(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,
@@ -165,11 +188,19 @@ lwm_status bwd_common(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, c
                       int S, int H, unsigned stages, void *ws, cudaStream_t stream, const DeviceInfo &d) {
   Problem p{B, S, H, d.num_sms};
   if (stages & LWM_BWD_DELTA) LWM_TRY(from_cuda(launch_delta(out, dout, lse, p, ws, stream)));
-  if (!(stages & (LWM_BWD_DKDV | LWM_BWD_DQ))) return LWM_OK;
+  if (!(stages & (LWM_BWD_DKDV | LWM_BWD_DQ | LWM_BWD_FUSED))) return LWM_OK;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_map(&tq, q, B, S, H) || !make_map(&tk, k, B, S, H) || !make_map(&tv, v, B, S, H) ||
       !make_map(&tdo, dout, B, S, H))
     return LWM_ERR_CUDA;
+  if (stages & LWM_BWD_FUSED) {
+    // the single-kernel pass streams the query side in 64-row halves
+    CUtensorMap tq64, tdo64, tacc;
+    if (!make_map(&tq64, q, B, S, H, 64) || !make_map(&tdo64, dout, B, S, H, 64) ||
+        !make_dqacc_map(&tacc, ws, B, S, H))
+      return LWM_ERR_CUDA;
+    LWM_TRY(from_cuda(launch_dkdvq(tq64, tk, tv, tdo64, tacc, dq, dk, dv, p, ws, stream)));
+  }
   if (stages & LWM_BWD_DKDV) LWM_TRY(from_cuda(launch_dkdv(tq, tk, tv, tdo, dk, dv, p, ws, stream)));
   if (stages & LWM_BWD_DQ) LWM_TRY(from_cuda(launch_dq(tq, tk, tv, tdo, dq, p, ws, stream)));
   return LWM_OK;
@@ -180,8 +211,9 @@ lwm_status check_stage_args(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16
                             const lwm_bf16 *dout, const float *lse, lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv,
                             int B, int S, int H, int D, unsigned stages, void *ws, size_t ws_bytes) {
   LWM_TRY(check_sizes(B, S, H, D));
-  if (stages == 0 || (stages & ~unsigned(LWM_BWD_ALL))) return LWM_ERR_INVALID_ARG;
-  const void *need16[8];
+  if (stages == 0 || (stages & ~unsigned(LWM_BWD_ALL | LWM_BWD_FUSED))) return LWM_ERR_INVALID_ARG;
+  if ((stages & LWM_BWD_FUSED) && (stages & (LWM_BWD_DKDV | LWM_BWD_DQ))) return LWM_ERR_INVALID_ARG;
+  const void *need16[10];
   int n = 0;
   if (stages & LWM_BWD_DELTA) {
     if (!lse) return LWM_ERR_INVALID_ARG;
@@ -189,22 +221,22 @@ lwm_status check_stage_args(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16
     need16[n++] = out;
     need16[n++] = dout;
   }
-  if (stages & (LWM_BWD_DKDV | LWM_BWD_DQ)) {
+  if (stages & (LWM_BWD_DKDV | LWM_BWD_DQ | LWM_BWD_FUSED)) {
     need16[n++] = q;
     need16[n++] = k;
     need16[n++] = v;
     need16[n++] = dout;
   }
-  if (stages & LWM_BWD_DKDV) {
+  if (stages & (LWM_BWD_DKDV | LWM_BWD_FUSED)) {
     need16[n++] = dk;
     need16[n++] = dv;
   }
-  if (stages & LWM_BWD_DQ) need16[n++] = dq;
+  if (stages & (LWM_BWD_DQ | LWM_BWD_FUSED)) need16[n++] = dq;
   for (int i = 0; i < n; ++i) {
     if (!need16[i]) return LWM_ERR_INVALID_ARG;
     if (!aligned16(need16[i])) return LWM_ERR_ALIGNMENT;
   }
-  return check_workspace(ws, ws_bytes, B, S, H);
+  return check_workspace(ws, ws_bytes, B, S, H, (stages & LWM_BWD_FUSED) != 0);
 }
 
 }  // namespace
@@ -232,12 +264,17 @@ size_t lwm_attn_workspace_size(int B, int S, int H, int D) {
   return Workspace::layout(B, S, H).total;
 }
 
+size_t lwm_attn_workspace_size_fwd(int B, int S, int H, int D) {
+  if (check_sizes(B, S, H, D) != LWM_OK) return 0;
+  return Workspace::layout(B, S, H).off_dqacc;
+}
+
 lwm_status lwm_attn_prepare(const int32_t *seg_ids, const int32_t *pos, int B, int S, int H, int D,
                             int kv_chunks, void *workspace, size_t workspace_bytes, lwm_stream stream) {
   LWM_TRY(check_sizes(B, S, H, D));
   if (kv_chunks < 1) return LWM_ERR_INVALID_ARG;
   LWM_TRY(check_seg_args(seg_ids, pos));
-  LWM_TRY(check_workspace(workspace, workspace_bytes, B, S, H));
+  LWM_TRY(check_workspace(workspace, workspace_bytes, B, S, H, false));
   DeviceInfo d;
   LWM_TRY(device_info(d));
   return prepare_impl(seg_ids, pos, B, S, H, kv_chunks, workspace, stream);
@@ -279,7 +316,8 @@ lwm_status lwm_attn_bwd(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
   DeviceInfo d;
   LWM_TRY(device_info(d));
   LWM_TRY(prepare_impl(seg_ids, pos, B, S, H, 1, workspace, stream));
-  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, LWM_BWD_ALL, workspace, stream, d);
+  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, LWM_BWD_DELTA | LWM_BWD_FUSED, workspace, stream,
+                    d);
 }
 
 lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,
@@ -289,7 +327,8 @@ lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm
   LWM_TRY(check_bwd_args(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, D, workspace, workspace_bytes));
   DeviceInfo d;
   LWM_TRY(device_info(d));
-  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, LWM_BWD_ALL, workspace, stream, d);
+  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, LWM_BWD_DELTA | LWM_BWD_FUSED, workspace, stream,
+                    d);
 }
 
 lwm_status lwm_attn_bwd_stages(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,

@@ -37,11 +37,14 @@ enum HeaderWord {
   HDR_DONE_DKDV = 7,
   HDR_TICKET_DQ = 8,
   HDR_DONE_DQ = 9,
+  HDR_TICKET_FUSED = 10,
+  HDR_DONE_FUSED = 11,
   HDR_WORDS = 64
 };
 
 struct Workspace {
-  size_t off_hdr, off_lo, off_kend, off_list_fwd, off_list_kv, off_list_q, off_delta, off_lse2, total;
+  size_t off_hdr, off_lo, off_kend, off_list_fwd, off_list_kv, off_list_q, off_delta, off_lse2, off_dqacc, total;
+  size_t dqacc_bytes;
   int nT, nP, S_pad;   // S_pad = nT * BM: per-row stride of lo, delta and lse2
 
   __host__ __device__ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -61,6 +64,9 @@ struct Workspace {
     // backward row terms, fp32 [B, H, nT * BM] (rows padded to whole tiles)
     w.off_delta = o;    o += align256(size_t(B) * H * w.S_pad * 4);
     w.off_lse2 = o;     o += align256(size_t(B) * H * w.S_pad * 4);
+    // fp32 dQ accumulator of the single-kernel backward pass, [B, H, S_pad, D]
+    w.dqacc_bytes = size_t(B) * H * w.S_pad * HD * 4;
+    w.off_dqacc = o;    o += align256(w.dqacc_bytes);
     w.total = o;
     return w;
   }
@@ -255,6 +261,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v) {
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
       "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v) {

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(META_THREADS) meta_sort_kernel(const int *__re
 
   if (which == 0 && threadIdx.x == 0) {
     hdr[HDR_KV_CHUNK] = kv_chunk;
-    for (int w = HDR_TICKET_FWD; w <= HDR_DONE_DQ; ++w) hdr[w] = 0;
+    for (int w = HDR_TICKET_FWD; w <= HDR_DONE_FUSED; ++w) hdr[w] = 0;
   }
   for (int k = threadIdx.x; k < NBINS; k += META_THREADS) hist[k] = 0;
   __syncthreads();

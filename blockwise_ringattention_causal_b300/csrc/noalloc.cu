@@ -58,8 +58,9 @@ extern "C" lwm_status lwm_attn_fwd_noalloc(const lwm_bf16 *q, const lwm_bf16 *k,
   const long long nT = (S + BM - 1) / BM;
   if (static_cast<long long>(B) * ((nT + 1) / 2) * H >= (1ll << 31)) return LWM_ERR_INVALID_ARG;
   // The forward pass uses only the part of the workspace in front of the backward
-  // rows; its size does not depend on H, and the layout with H = 1 covers it.
-  if (Workspace::layout(B, S, 1).total > NOALLOC_BYTES) return LWM_ERR_INVALID_ARG;
+  // rows; its size does not depend on H, and the layout with H = 1 (without the dQ
+  // accumulator of the backward pass) covers it.
+  if (Workspace::layout(B, S, 1).off_dqacc > NOALLOC_BYTES) return LWM_ERR_INVALID_ARG;
   if (!q || !k || !v || !out || !lse) return LWM_ERR_INVALID_ARG;
   const auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   const auto a4 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };

@@ -73,8 +73,15 @@ typedef enum {
 
 /* Bytes of device workspace needed for problems of this shape (0 on bad sizes).
  * The workspace holds the per-token segment starts, per-tile ranges, the schedule's
- * work lists and tickets, the error word and the backward row dots (fp32 [B,H,S]). */
+ * work lists and tickets, the error word, the backward row dots (fp32 [B,H,S]) and,
+ * at its end, the fp32 dQ accumulator of the single-kernel backward pass
+ * (4 * B * H * S * D bytes, S rounded up to a multiple of 128). */
 size_t lwm_attn_workspace_size(int B, int S, int H, int D);
+
+/* The leading part of that workspace which every call except the single-kernel
+ * backward pass uses (no dQ accumulator): enough for lwm_attn_prepare, the forward
+ * entry points and the LWM_BWD_DELTA / LWM_BWD_DKDV / LWM_BWD_DQ stages. */
+size_t lwm_attn_workspace_size_fwd(int B, int S, int H, int D);
 
 /* Metadata pre-pass alone: validates seg_ids/pos and writes segment starts, per-tile
  * key/query ranges and longest-first work lists into `workspace`. The *_prepared
@@ -107,8 +114,12 @@ lwm_status lwm_attn_fwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm
                                  void *workspace, size_t workspace_bytes, lwm_stream stream);
 
 /* Backward pass: metadata pre-pass, the row-dot pre-pass delta_i = dout_i . out_i,
- * then the dK/dV kernel and the dQ kernel. `out` and `lse` are the forward outputs.
- * dq, dk, dv are fully overwritten (no accumulation into existing values). */
+ * then the single-kernel backward pass (LWM_BWD_FUSED below). `out` and `lse` are the
+ * forward outputs. dq, dk, dv are fully overwritten (no accumulation into existing
+ * values). dk and dv are bitwise reproducible; dq is summed in fp32 in an order that
+ * depends on scheduling (run-to-run differences at the level of fp32 rounding before
+ * the bf16 conversion). LWM_BWD_ALL through lwm_attn_bwd_stages gives a bitwise
+ * reproducible dq. The workspace must have lwm_attn_workspace_size() bytes. */
 lwm_status lwm_attn_bwd(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
                         const lwm_bf16 *out, const lwm_bf16 *dout, const float *lse,
                         const int32_t *seg_ids, const int32_t *pos,
@@ -116,7 +127,8 @@ lwm_status lwm_attn_bwd(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
                         int B, int S, int H, int D, void *workspace, size_t workspace_bytes,
                         lwm_stream stream);
 
-/* Backward pass reusing the metadata of a previous lwm_attn_prepare in `workspace`. */
+/* Backward pass reusing the metadata of a previous lwm_attn_prepare in `workspace`
+ * (same stages as lwm_attn_bwd: LWM_BWD_DELTA | LWM_BWD_FUSED). */
 lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
                                  const lwm_bf16 *out, const lwm_bf16 *dout, const float *lse,
                                  lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv,
@@ -128,15 +140,21 @@ typedef enum {
   LWM_BWD_DELTA = 1,  /* row dots delta = rowsum(dout * out) and lse rows, into the workspace */
   LWM_BWD_DKDV = 2,   /* dk, dv (needs LWM_BWD_DELTA's results in the workspace) */
   LWM_BWD_DQ = 4,     /* dq (needs LWM_BWD_DELTA's results in the workspace) */
-  LWM_BWD_ALL = 7
+  LWM_BWD_ALL = 7,    /* the three stages above: every gradient bitwise reproducible */
+  LWM_BWD_FUSED = 8   /* dk, dv and dq in one kernel from one recomputation of the
+                         probabilities (5 tensor-core products per tile pair instead of
+                         7): dq is accumulated in fp32 in the workspace's dQ accumulator
+                         (zeroed by the stage itself) and then converted to bf16. Needs
+                         LWM_BWD_DELTA's results; cannot be combined with DKDV or DQ */
 } lwm_bwd_stage;
 
-/* Runs the selected backward stages in the order delta, dK/dV, dQ, reusing the
+/* Runs the selected backward stages in the order delta, fused, dK/dV, dQ, reusing the
  * metadata of a previous lwm_attn_prepare. After the delta stage has completed, the
  * dK/dV and dQ stages only read the workspace (each has its own scheduler ticket), so
  * a caller may run them on two streams. Pointers that no selected stage touches may
  * be NULL (delta: out, dout, lse; dK/dV: q, k, v, dout, dk, dv; dQ: q, k, v, dout,
- * dq). lwm_attn_bwd_prepared is stages = LWM_BWD_ALL. */
+ * dq; fused: q, k, v, dout, dq, dk, dv). The workspace needs lwm_attn_workspace_size()
+ * bytes when LWM_BWD_FUSED is selected, lwm_attn_workspace_size_fwd() bytes otherwise. */
 lwm_status lwm_attn_bwd_stages(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
                                const lwm_bf16 *out, const lwm_bf16 *dout, const float *lse,
                                lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv,

@@ -18,15 +18,20 @@ from tests._parity import GRAD_REL, f64, rel_l2
 pytestmark = pytest.mark.gpu
 
 
-def run_fwd_bwd(x):
+def run_fwd_bwd(x, deterministic=False):
     out, lse, ws = lwm.forward(x["q"], x["k"], x["v"], x.get("seg"), x.get("pos"))
-    dq, dk, dv = lwm.backward(x["q"], x["k"], x["v"], out, x["dout"], lse, x.get("seg"), x.get("pos"), ws)
+    dq, dk, dv = lwm.backward(x["q"], x["k"], x["v"], out, x["dout"], lse, x.get("seg"), x.get("pos"), ws,
+                              deterministic=deterministic)
     assert lwm.lwm_attn_check(ws) == 0
     return out, lse, dq, dk, dv
 
 
-def check_full(x, what):
-    _, _, dq, dk, dv = run_fwd_bwd(x)
+# both backward paths: the single-kernel one (default) and the separate dK/dV + dQ kernels
+PATHS = pytest.mark.parametrize("deterministic", [False, True], ids=["fused", "separate"])
+
+
+def check_full(x, what, deterministic=False):
+    _, _, dq, dk, dv = run_fwd_bwd(x, deterministic)
     seg = x["seg"].cpu().numpy() if x.get("seg") is not None else None
     refs = oracle.attention_backward(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["dout"]), seg)
     floor = 1e-3 * float(np.linalg.norm(f64(x["dout"])))
@@ -35,46 +40,72 @@ def check_full(x, what):
     return errs
 
 
-def test_packed_three_documents_s1k(cuda_device):
-    check_full(I.make_inputs(I.workload(1), cuda_device), "packed 300/424/300")
+@PATHS
+def test_packed_three_documents_s1k(cuda_device, deterministic):
+    check_full(I.make_inputs(I.workload(1), cuda_device), "packed 300/424/300", deterministic)
 
 
 @pytest.mark.parametrize("S,lengths", [
     (1, [[1]]), (127, [[127]]), (129, [[129]]), (300, [[100, 1, 199]]), (257, [[200, 30]]),
     (640, [[128, 128, 384]]), (500, [[7] * 70 + [10]]), (1000, [[1000]]),
 ])
-def test_ragged_and_packed_shapes(cuda_device, S, lengths):
-    check_full(I.make_inputs(I.custom(1, S, 3, 128, lengths, seed=S), cuda_device), f"S={S}")
+@PATHS
+def test_ragged_and_packed_shapes(cuda_device, S, lengths, deterministic):
+    check_full(I.make_inputs(I.custom(1, S, 3, 128, lengths, seed=S), cuda_device), f"S={S}", deterministic)
 
 
-def test_batch_rows_with_padding(cuda_device):
+@PATHS
+def test_batch_rows_with_padding(cuda_device, deterministic):
     x = I.make_inputs(I.custom(3, 700, 2, 128, [[700], [50, 650], [300, 300, 64]], seed=5), cuda_device)
-    check_full(x, "B=3")
-    _, _, dq, dk, dv = run_fwd_bwd(x)
+    check_full(x, "B=3", deterministic)
+    _, _, dq, dk, dv = run_fwd_bwd(x, deterministic)
     for g in (dq, dk, dv):
         assert torch.all(g[2, 664:] == 0)
 
 
-def test_backward_is_deterministic(cuda_device):
+def test_separate_path_is_deterministic(cuda_device):
     x = I.make_inputs(I.custom(1, 3000, 4, 128, [[1000, 2000]], seed=8), cuda_device)
-    a = run_fwd_bwd(x)
-    b = run_fwd_bwd(x)
+    a = run_fwd_bwd(x, deterministic=True)
+    b = run_fwd_bwd(x, deterministic=True)
     for u, w in zip(a, b):
         assert torch.equal(u, w)
 
 
-def test_large_scores_stay_finite(cuda_device):
+def test_fused_path_repeats_dk_dv_exactly(cuda_device):
+    """dk and dv of the single-kernel path are bitwise reproducible; dq is summed in fp32
+    in a scheduling-dependent order, so two runs agree to fp32 rounding before the bf16
+    conversion: at most one bf16 unit in the last place apart."""
+    x = I.make_inputs(I.custom(1, 3000, 4, 128, [[1000, 2000]], seed=8), cuda_device)
+    a = run_fwd_bwd(x)
+    b = run_fwd_bwd(x)
+    for u, w in zip(a[:2] + a[3:], b[:2] + b[3:]):
+        assert torch.equal(u, w)
+    dq_a, dq_b = a[2].float(), b[2].float()
+    bound = torch.maximum(dq_a.abs(), dq_b.abs()) * 2.0 ** -7 + 1e-5 * float(dq_a.abs().max())
+    assert torch.all((dq_a - dq_b).abs() <= bound)
+
+
+def test_fused_and_separate_paths_agree(cuda_device):
+    x = I.make_inputs(I.custom(2, 1500, 3, 128, [[700, 800], [1500]], seed=11), cuda_device)
+    f = run_fwd_bwd(x)
+    d = run_fwd_bwd(x, deterministic=True)
+    for name, g, h in zip(("dq", "dk", "dv"), f[2:], d[2:]):
+        assert rel_l2(f64(g), f64(h)) <= 5e-3, name
+
+
+@PATHS
+def test_large_scores_stay_finite(cuda_device, deterministic):
     x = I.make_inputs(I.custom(1, 512, 2, 128, [[512]], seed=9), cuda_device)
     x["q"] = (x["q"].float() * 30).to(torch.bfloat16)
-    _, _, dq, dk, dv = run_fwd_bwd(x)
+    _, _, dq, dk, dv = run_fwd_bwd(x, deterministic)
     for g in (dq, dk, dv):
         assert torch.isfinite(g.float()).all()
 
 
-def _sampled_bwd(config, cuda_device, key_heads=(0, 17)):
+def _sampled_bwd(config, cuda_device, key_heads=(0, 17), deterministic=False):
     w = I.workload(config)
     x = I.make_inputs(w, cuda_device)
-    _, _, dq, dk, dv = run_fwd_bwd(x)
+    _, _, dq, dk, dv = run_fwd_bwd(x, deterministic)
     rows = I.sample_rows(w.S)
     keys = I.sample_rows(w.S, seed=2)
     seg = x["seg"].cpu().numpy()
@@ -96,8 +127,9 @@ def _sampled_bwd(config, cuda_device, key_heads=(0, 17)):
     assert max(e_dq, e_dk, e_dv) <= GRAD_REL, f"config {config}: dq {e_dq:.2e} dk {e_dk:.2e} dv {e_dv:.2e}"
 
 
-def test_causal_s32k_sampled(cuda_device):
-    _sampled_bwd(2, cuda_device)
+@PATHS
+def test_causal_s32k_sampled(cuda_device, deterministic):
+    _sampled_bwd(2, cuda_device, deterministic=deterministic)
 
 
 def test_packed_mixed_s64k_sampled(cuda_device):
