@@ -91,12 +91,12 @@ bool make_map(CUtensorMap *m, const void *ptr, int B, int S, int H, int rows = B
 }
 
 // The fp32 dQ accumulator [B * H * S_pad rows, 128 dims] of the workspace, written by
-// tensor reduce-add copies of 16-row x 32-dim boxes.
+// tensor reduce-add copies of 8-row x 32-dim boxes.
 bool make_dqacc_map(CUtensorMap *m, void *ws, int B, int S, int H) {
   const Workspace w = Workspace::layout(B, S, H);
   cuuint64_t dims[2] = {cuuint64_t(HD), cuuint64_t(B) * H * w.S_pad};
   cuuint64_t strides[1] = {cuuint64_t(HD) * 4};
-  cuuint32_t box[2] = {32, 16};
+  cuuint32_t box[2] = {32, 8};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, static_cast<char *>(ws) + w.off_dqacc, dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -194,12 +194,9 @@ lwm_status bwd_common(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, c
       !make_map(&tdo, dout, B, S, H))
     return LWM_ERR_CUDA;
   if (stages & LWM_BWD_FUSED) {
-    // the single-kernel pass streams the query side in 64-row halves
-    CUtensorMap tq64, tdo64, tacc;
-    if (!make_map(&tq64, q, B, S, H, 64) || !make_map(&tdo64, dout, B, S, H, 64) ||
-        !make_dqacc_map(&tacc, ws, B, S, H))
-      return LWM_ERR_CUDA;
-    LWM_TRY(from_cuda(launch_dkdvq(tq64, tk, tv, tdo64, tacc, dq, dk, dv, p, ws, stream)));
+    CUtensorMap tacc;
+    if (!make_dqacc_map(&tacc, ws, B, S, H)) return LWM_ERR_CUDA;
+    LWM_TRY(from_cuda(launch_dkdvq(tq, tk, tv, tdo, tacc, dq, dk, dv, p, ws, stream)));
   }
   if (stages & LWM_BWD_DKDV) LWM_TRY(from_cuda(launch_dkdv(tq, tk, tv, tdo, dk, dv, p, ws, stream)));
   if (stages & LWM_BWD_DQ) LWM_TRY(from_cuda(launch_dq(tq, tk, tv, tdo, dq, p, ws, stream)));

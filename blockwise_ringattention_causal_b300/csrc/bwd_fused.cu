@@ -9,75 +9,73 @@
 //   p_ij = exp(s_ij - lse_i),  dp_ij = dout_i . v_j,  ds_ij = p_ij (dp_ij - delta_i)
 //   dv_j = sum_i p_ij dout_i,  dk_j = sum_i ds_ij q_i / sqrt(D),  dq_i = sum_j ds_ij k_j / sqrt(D)
 //
-// Item: (b, h, 128-key tile), taken longest-first through an atomic ticket by one
-// persistent CTA per SM. K and V of the tile stay resident in shared memory; the
-// query rows that see the tile stream through in 64-row halves u = 0, 1, 2, ...
-// (Q, dO and the rows' lo / lse / delta terms). Per half u, with region r = u & 1:
-//   S^T_u  = K . Q_u^T, dP^T_u = V . dO_u^T          (128 keys x 64 queries, fp32 TMEM)
-//   P^T, dS^T (softmax warpgroup r, one key row per thread) -> bf16 TMEM, and dS^T
-//   also into shared memory
-//   dV += P^T_u . dO_u,  dK += dS^T_u . Q_u           (TMEM accumulators)
-//   dQ^T_u = K^T . dS^T_u                             (128 dims x 64 queries, fp32 TMEM)
-// and four readout warps, each owning 32 of the head dims, stage dQ^T_u in shared
-// memory as [16 queries x 32 dims] fp32 blocks that tensor bulk reduce-add copies add
-// into an fp32 accumulator [B, H, S_pad, D] in global memory (the addition happens in
-// L2). A final pass converts it to bf16 dq. The
-// order of the fp32 additions depends on scheduling, so dq is not bitwise reproducible
-// from run to run (dk and dv are).
+// Item: (b, h, 128-key tile), taken through an atomic ticket by one persistent CTA per
+// SM (items of one head are consecutive, longest first, so that the CTAs running at
+// the same time share their query-side tiles in L2). K and V of the tile stay
+// resident in shared memory; the 128-row query tiles j that see it stream through
+// (Q_j in a ring of two buffers with its rows' lo / lse / delta terms, dO_j in one
+// buffer). Per tile j, every product is 128 x 128 x 128:
+//   S^T  = K . Q_j^T   -> TMEM region A         dP^T = V . dO_j^T -> TMEM region B
+//   P^T  = exp2(S^T c - lse2)  (softmax warps)  -> bf16 over region A
+//   dV  += P^T . dO_j                           (needs only P: issued before dS is ready)
+//   dS^T = P^T (dP^T - delta)  (softmax warps)  -> bf16 over region A, and into shared memory
+//   dK  += dS^T . Q_j,   dQ^T = K^T . dS^T      -> dQ^T into region B
+// and the softmax warps then move dQ^T out of TMEM and add it, through shared staging
+// buffers and tensor bulk reduce-add copies (performed in L2), into an fp32
+// accumulator [B, H, S_pad, D]. A final pass converts that to bf16 dq. The order of
+// the fp32 additions depends on scheduling, so dq is not bitwise reproducible from run
+// to run (dk and dv are).
 //
-// Warp roles: 0-3 softmax of region 0, 4-7 softmax of region 1, 8-11 dQ readout (warp
-// w reads TMEM lanes 32 (w % 4) ...), 12 TMA producer, 13 MMA issuer (128 registers
-// per thread: 14 warps put 4 warps on some SM sub-partitions).
-// TMEM columns (fp32):
-//   r*128 + [0, 64)   S^T_r, then P^T_r and dS^T_r (bf16, 8 columns per 16 queries,
-//                     alternating: P^T q0-15, dS^T q0-15, P^T q16-31, ...)
-//   r*128 + [64, 128) dP^T_r, then dQ^T_r
-//   256 dV, 384 dK
+// The tensor core runs S^T(j+1) while the softmax warps take dQ^T(j) out, dP^T(j+1)
+// while they compute P(j+1), and dV(j+1) while they compute dS(j+1), so that it has
+// work queued through each softmax phase.
+//
+// Warp roles: 0-3 and 4-7 two warpgroups, warpgroup w owning query columns
+// [64 w, 64 w + 64) of every tile (thread = key row = TMEM lane); 8 TMA producer;
+// 9 MMA issuer; 10-11 idle (3 warps per SM sub-partition: 168 registers per thread).
+// TMEM columns: A [0, 128), B [128, 256), dV [256, 384), dK [384, 512). In region A,
+// the 16-query chunk c (columns 16c .. 16c+15 of S^T) is overwritten by P^T of those
+// queries (bf16, columns 16c .. 16c+7) and then dS^T (16c+8 .. 16c+15).
 #include "common.cuh"
 #include "kernels.h"
 
 namespace lwm {
 namespace {
 
-constexpr int FB_WARPS = 14;
+constexpr int FB_WARPS = 12;
 constexpr int FB_THREADS = FB_WARPS * 32;
-constexpr int FB_READ0 = 8;
-constexpr int FB_PRODUCER = 12;
-constexpr int FB_MMA = 13;
-constexpr int QH = 64;                        // queries per streamed half tile
-constexpr int QH_BOX = QH * 128;              // 64 rows x 64 dims, 128B-swizzled: 8 KiB
-constexpr int QH_BYTES = 2 * QH_BOX;          // 64 rows x 128 dims: 16 KiB
-constexpr int RT_BYTES = QH * 4;              // 64 row terms (int32 / fp32)
-constexpr int FB_STAGES = 3;
-constexpr int FB_STAGE_BYTES = 2 * QH_BYTES + 3 * RT_BYTES;   // Q, dO, lo, lse2, delta
-constexpr int FB_STAGE_STRIDE = (FB_STAGE_BYTES + 1023) & ~1023;
-constexpr int DS_BYTES = BN * QH * 2;         // dS^T: 128 keys x 64 queries bf16
-constexpr int FB_SM_K = 0, FB_SM_V = TILE_BYTES, FB_SM_DS = 2 * TILE_BYTES;
-constexpr int FB_SM_ST = FB_SM_DS + 2 * DS_BYTES;
-constexpr int RED_Q = 16;                     // queries per dQ reduction block
-constexpr int RED_BLOCK = RED_Q * 32 * 4;     // [16 queries x 32 dims] fp32 of one warp: 2 KiB
-constexpr int FB_SM_RED = FB_SM_ST + FB_STAGES * FB_STAGE_STRIDE;   // 4 warps x 2 buffers
-constexpr int FB_SM_BAR = FB_SM_RED + 4 * 2 * RED_BLOCK;
+constexpr int FB_PRODUCER = 8;
+constexpr int FB_MMA = 9;
+constexpr int RT_BYTES = BM * 4;                // 128 row terms (int32 / fp32)
+constexpr int DS_BYTES = BN * BM * 2;           // dS^T staging: 128 keys x 128 queries bf16
+constexpr int RED_Q = 8;                        // queries per dQ reduction block
+constexpr int RED_BLOCK = RED_Q * 32 * 4;       // [8 queries x 32 dims] fp32: 1 KiB
+// shared memory map (bytes; tiles 1024-aligned)
+constexpr int FB_SM_K = 0;
+constexpr int FB_SM_V = FB_SM_K + TILE_BYTES;
+constexpr int FB_SM_Q = FB_SM_V + TILE_BYTES;             // 2 Q buffers
+constexpr int FB_SM_DO = FB_SM_Q + 2 * TILE_BYTES;        // 1 dO buffer
+constexpr int FB_SM_DS = FB_SM_DO + TILE_BYTES;           // dS^T, two 64-query halves of 16 KiB
+constexpr int FB_SM_RED = FB_SM_DS + DS_BYTES;            // 8 warps x 2 reduction buffers
+constexpr int FB_SM_RT = FB_SM_RED + 8 * 2 * RED_BLOCK;   // row terms of the 2 Q buffers
+constexpr int FB_SM_BAR = FB_SM_RT + 2 * 3 * RT_BYTES;
 
-constexpr uint32_t COL_DV = 256, COL_DK = 384;
-constexpr uint32_t IDESC_ST = idesc_bf16(BN, QH, false, false);   // [128 x 64] = A . B^T, both K-major
-constexpr uint32_t IDESC_ACC = idesc_bf16(BN, HD, false, true);   // acc += X(tmem) . Y (Y MN-major)
-constexpr uint32_t IDESC_DQ = idesc_bf16(HD, QH, true, true);     // dQ^T = K^T . dS^T, both MN-major
-
-__device__ __forceinline__ uint32_t col_s(int r) { return uint32_t(r) * 128u; }
-__device__ __forceinline__ uint32_t col_dp(int r) { return uint32_t(r) * 128u + 64u; }
+constexpr uint32_t COL_A = 0, COL_B = 128, COL_DV = 256, COL_DK = 384;
+constexpr uint32_t IDESC_KM = idesc_bf16(128, 128, false, false);   // D = A . B^T, both K-major
+constexpr uint32_t IDESC_TS = idesc_bf16(128, 128, false, true);    // acc += X(tmem) . Y (Y MN-major)
+constexpr uint32_t IDESC_MN = idesc_bf16(128, 128, true, true);     // dQ^T = K^T . dS^T, both MN-major
 
 struct FbBars {
-  uint64_t st_full[FB_STAGES], st_empty[FB_STAGES];
+  uint64_t q_full[2], q_empty[2], do_full, do_empty;
   uint64_t own_full, own_empty;
-  uint64_t s_full[2], p_full[2], dq_full[2], dq_empty[2];
+  uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty;
   uint64_t acc_full, acc_empty;
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   int item[2];
   uint32_t tmem_base;
   int abort;
-  int fill, use, own_issued, own_used;
+  int q_fill, q_use, do_fill, do_use, own_issued, own_used;
 };
 constexpr int FB_SMEM = FB_SM_BAR + int(sizeof(FbBars)) + 1024;
 static_assert(FB_SMEM <= 232448, "shared memory budget of one CTA");
@@ -85,13 +83,12 @@ static_assert(FB_SMEM <= 232448, "shared memory budget of one CTA");
 struct FbArgs {
   const int *lo;       // [B, S_pad]
   const int *kend;     // [B, nT]
-  const int *list;     // key-tile work list (b * nT + tile), longest first
+  const int *list;     // key tiles (b * nT + tile), longest first
   const float *delta;  // [B, H, S_pad]
   const float *lse2;   // [B, H, S_pad]: lse * log2(e), +inf where nothing is visible
-  float *dqacc;        // [B, H, S_pad, D] fp32, zero on entry
   int *hdr;
   __nv_bfloat16 *dk, *dv;
-  int B, S, H, nT, S_pad, n_items;
+  int B, S, H, nT, S_pad, n_list, n_items;
   float scale_log2;    // log2(e) / sqrt(D)
   float inv_sqrt_d;
 };
@@ -100,9 +97,10 @@ struct FbItem {
   int b, h, tile;
 };
 
+// Items of one head are consecutive (head-major), each head's key tiles longest first.
 __device__ __forceinline__ FbItem fb_decode(const FbArgs &a, int item) {
-  const int e = a.list[item / a.H];
-  return {e / a.nT, item % a.H, e % a.nT};
+  const int e = a.list[item % a.n_list];
+  return {e / a.nT, item / a.n_list, e % a.nT};
 }
 
 // Query tiles that see key tile `tile`: [tile, (kend - 1) / BM].
@@ -117,317 +115,42 @@ __device__ __forceinline__ TileRange fb_range(const FbArgs &a, const FbItem &I) 
   return r;
 }
 
-__device__ __forceinline__ int fb_halves(const TileRange &R) { return R.empty() ? 0 : 2 * (R.last - R.first + 1); }
+__device__ __forceinline__ int fb_tiles(const TileRange &R) { return R.empty() ? 0 : R.last - R.first + 1; }
 
-// D[128 keys x 64 queries] = A[128 keys x 128 dims] . B[64 queries x 128 dims]^T.
-// A is a resident tile (its two 64-dim boxes HALF_BYTES apart), B a streamed half
-// tile (boxes QH_BOX apart); both K-major, 128B-swizzled.
-__device__ __forceinline__ void issue_st(uint32_t d_tmem, uint32_t a_s, uint32_t b_s) {
+// D[128 x 128] = A[128 rows x 128 dims] . B[128 rows x 128 dims]^T; both operands are
+// 128-row tiles stored as two 64-dim 128B-swizzled boxes HALF_BYTES apart (K-major).
+__device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t a_s, uint32_t b_s) {
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
-    const uint32_t in_row = uint32_t(kk & 3) * 32;
-    mma_ss(d_tmem, sdesc_sw128(a_s + uint32_t(kk >> 2) * HALF_BYTES + in_row, 16, 1024),
-           sdesc_sw128(b_s + uint32_t(kk >> 2) * QH_BOX + in_row, 16, 1024), IDESC_ST, kk > 0);
+    const uint32_t off = uint32_t(kk >> 2) * HALF_BYTES + uint32_t(kk & 3) * 32;
+    mma_ss(d_tmem, sdesc_sw128(a_s + off, 16, 1024), sdesc_sw128(b_s + off, 16, 1024), IDESC_KM, kk > 0);
   }
 }
 
-// acc[128 keys x 128 dims] (+)= X[128 keys x 64 queries] (bf16 in TMEM) . Y[64 x 128]
-// with Y a streamed half tile read MN-major (dims contiguous; 16 rows = two 8-row
-// groups of 1024 bytes; the 64-dim boxes QH_BOX apart). X's 16-query blocks (8 packed
-// columns each) sit 16 columns apart: P^T and dS^T blocks alternate.
-__device__ __forceinline__ void issue_acc(uint32_t acc, uint32_t x_tmem, uint32_t y_s, bool accumulate) {
+// acc[128 keys x 128 dims] (+)= X[128 keys x 128 queries] (bf16 in TMEM; the 16-query
+// block kk at column 16 kk of x_tmem) . Y[128 queries x 128 dims] read MN-major (dims
+// contiguous: 16 rows = two 8-row groups of 1024 bytes; the 64-dim boxes HALF_BYTES
+// apart).
+__device__ __forceinline__ void issue_ts(uint32_t acc, uint32_t x_tmem, uint32_t y_s, bool accumulate) {
 #pragma unroll
-  for (int kk = 0; kk < QH / 16; ++kk)
-    mma_ts(acc, x_tmem + uint32_t(kk) * 16, sdesc_sw128(y_s + uint32_t(kk) * 2048, QH_BOX, 1024), IDESC_ACC,
+  for (int kk = 0; kk < BM / 16; ++kk)
+    mma_ts(acc, x_tmem + uint32_t(kk) * 16, sdesc_sw128(y_s + uint32_t(kk) * 2048, HALF_BYTES, 1024), IDESC_TS,
            (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// dQ^T[128 dims x 64 queries] = K^T[128 dims x 128 keys] . dS^T[128 keys x 64 queries].
+// dQ^T[128 dims x 128 queries] = K^T[128 dims x 128 keys] . dS^T[128 keys x 128 queries].
 // Both operands are read MN-major: K as stored (dims contiguous, 64-dim boxes
-// HALF_BYTES apart), dS^T as written by the softmax warps (queries contiguous, one
-// 128-byte swizzled row per key).
+// HALF_BYTES apart), dS^T as the softmax warps write it (queries contiguous, 128-byte
+// swizzled rows, one per key; the 64-query halves DS_BYTES / 2 apart).
 __device__ __forceinline__ void issue_dqt(uint32_t d_tmem, uint32_t k_s, uint32_t ds_s) {
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk)
     mma_ss(d_tmem, sdesc_sw128(k_s + uint32_t(kk) * 2048, HALF_BYTES, 1024),
-           sdesc_sw128(ds_s + uint32_t(kk) * 2048, DS_BYTES, 1024), IDESC_DQ, kk > 0);
+           sdesc_sw128(ds_s + uint32_t(kk) * 2048, DS_BYTES / 2, 1024), IDESC_MN, kk > 0);
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ bool fb_wait_plain(uint64_t *bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
-  return true;
-}
-
-__device__ __forceinline__ void fb_load_half(const CUtensorMap *m, uint64_t *bar, uint8_t *dst, int h, int row0,
-                                             int b) {
-  tma_load_4d(m, bar, dst, 0, h, row0, b);
-  tma_load_4d(m, bar, dst + QH_BOX, 64, h, row0, b);
-}
-
-__device__ __forceinline__ void fb_load_tile(const CUtensorMap *m, uint64_t *bar, uint8_t *dst, int h, int row0,
-                                             int b) {
-  tma_load_4d(m, bar, dst, 0, h, row0, b);
-  tma_load_4d(m, bar, dst + HALF_BYTES, 64, h, row0, b);
-}
-
-// ----------------------------------------------------------------------------- roles
-__device__ __forceinline__ bool fb_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
-                            const CUtensorMap *tdo, const FbArgs &a, uint8_t *smem, FbBars *bars) {
-  volatile int *abort = &bars->abort;
-  int fill = 0, own = 0;
-  bool ok = true;
-  for (int it = 0;; ++it) {
-    const int slot = it & 1;
-    if (!(ok = mbar_wait(&bars->item_empty[slot], ((it >> 1) & 1) ^ 1, abort))) break;
-    const int t = atomicAdd(a.hdr + HDR_TICKET_FUSED, 1);
-    const int item = t < a.n_items ? t : -1;
-    bars->item[slot] = item;
-    mbar_arrive(&bars->item_full[slot]);
-    if (item < 0) break;
-    const FbItem I = fb_decode(a, item);
-    const TileRange R = fb_range(a, I);
-    const int n = fb_halves(R);
-    if (!(ok = mbar_wait(&bars->own_empty, (it & 1) ^ 1, abort))) break;
-    mbar_arrive_expect_tx(&bars->own_full, 2 * TILE_BYTES);
-    fb_load_tile(tk, &bars->own_full, smem + FB_SM_K, I.h, I.tile * BN, I.b);
-    fb_load_tile(tv, &bars->own_full, smem + FB_SM_V, I.h, I.tile * BN, I.b);
-    ++own;
-    const size_t rowbase = (size_t(I.b) * a.H + I.h) * a.S_pad;
-    for (int u = 0; u < n && ok; ++u) {
-      const int st = fill % FB_STAGES;
-      if (!(ok = mbar_wait(&bars->st_empty[st], ((fill / FB_STAGES) & 1) ^ 1, abort))) break;
-      mbar_arrive_expect_tx(&bars->st_full[st], FB_STAGE_BYTES);
-      uint8_t *dst = smem + FB_SM_ST + st * FB_STAGE_STRIDE;
-      const int row0 = (R.first + (u >> 1)) * BM + (u & 1) * QH;
-      fb_load_half(tq, &bars->st_full[st], dst, I.h, row0, I.b);
-      fb_load_half(tdo, &bars->st_full[st], dst + QH_BYTES, I.h, row0, I.b);
-      bulk_load(dst + 2 * QH_BYTES, a.lo + size_t(I.b) * a.S_pad + row0, RT_BYTES, &bars->st_full[st]);
-      bulk_load(dst + 2 * QH_BYTES + RT_BYTES, a.lse2 + rowbase + row0, RT_BYTES, &bars->st_full[st]);
-      bulk_load(dst + 2 * QH_BYTES + 2 * RT_BYTES, a.delta + rowbase + row0, RT_BYTES, &bars->st_full[st]);
-      ++fill;
-    }
-    if (!ok) break;
-  }
-  bars->fill = fill;
-  bars->own_issued = own;
-  return ok;
-}
-
-__device__ __forceinline__ bool fb_mma(const FbArgs &a, uint8_t *smem, FbBars *bars, uint32_t tmem, int lane) {
-  volatile int *abort = &bars->abort;
-  const uint32_t k_s = smem_u32(smem + FB_SM_K), v_s = smem_u32(smem + FB_SM_V);
-  const uint32_t ds0 = smem_u32(smem + FB_SM_DS), st0 = smem_u32(smem + FB_SM_ST);
-  int use = 0, own = 0;
-  uint32_t pf_par[2] = {0, 0}, de_par[2] = {0, 0}, ae_par = 1;
-  bool dq_pending[2] = {false, false};
-  bool ok = true;
-
-  for (int it = 0; ok; ++it) {
-    const int slot = it & 1;
-    if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
-    const int item = bars->item[slot];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
-    if (item < 0) break;
-    const FbItem I = fb_decode(a, item);
-    const int n = fb_halves(fb_range(a, I));
-    if (!(ok = mbar_wait(&bars->own_full, it & 1, abort))) break;
-    ++own;
-    tc_fence_after();
-    const int base = use;
-
-    // S^T and dP^T of half u into region u & 1. dP^T overwrites the region's dQ^T of
-    // two halves ago, so it waits until the readout warps have taken that out.
-    auto issue_sdp = [&](int u) -> bool {
-      const int r = u & 1, st = (base + u) % FB_STAGES;
-      if (!mbar_wait(&bars->st_full[st], ((base + u) / FB_STAGES) & 1, abort)) return false;
-      tc_fence_after();
-      const uint32_t q_s = st0 + st * FB_STAGE_STRIDE, do_s = q_s + QH_BYTES;
-      if (lane == 0) issue_st(tmem + col_s(r), k_s, q_s);
-      __syncwarp();
-      if (dq_pending[r]) {
-        if (!mbar_wait(&bars->dq_empty[r], de_par[r], abort)) return false;
-        de_par[r] ^= 1;
-        dq_pending[r] = false;
-        tc_fence_after();
-      }
-      if (lane == 0) {
-        issue_st(tmem + col_dp(r), v_s, do_s);
-        mma_commit(&bars->s_full[r]);
-      }
-      __syncwarp();
-      return true;
-    };
-
-    for (int u = 0; u < n && u < 2 && ok; ++u) ok = issue_sdp(u);
-    for (int u = 0; u < n && ok; ++u) {
-      const int r = u & 1, st = (base + u) % FB_STAGES;
-      const uint32_t q_s = st0 + st * FB_STAGE_STRIDE, do_s = q_s + QH_BYTES;
-      if (!(ok = mbar_wait(&bars->p_full[r], pf_par[r], abort))) break;
-      pf_par[r] ^= 1;
-      if (u == 0) {
-        if (!(ok = mbar_wait(&bars->acc_empty, ae_par, abort))) break;
-        ae_par ^= 1;
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        issue_acc(tmem + COL_DV, tmem + col_s(r), do_s, u > 0);          // dV += P^T dO
-        issue_acc(tmem + COL_DK, tmem + col_s(r) + 8, q_s, u > 0);      // dK += dS^T Q
-        issue_dqt(tmem + col_dp(r), k_s, ds0 + r * DS_BYTES);            // dQ^T = K^T dS^T
-        mma_commit(&bars->dq_full[r]);
-        mma_commit(&bars->st_empty[st]);
-      }
-      __syncwarp();
-      dq_pending[r] = true;
-      if (u + 2 < n) ok = issue_sdp(u + 2);
-    }
-    if (!ok) break;
-    use = base + n;
-    if (lane == 0) {
-      if (n > 0) mma_commit(&bars->acc_full);
-      mma_commit(&bars->own_empty);
-    }
-    __syncwarp();
-  }
-  if (lane == 0) {
-    bars->use = use;
-    bars->own_used = own;
-  }
-  return ok;
-}
-
-// Softmax warpgroup of region r: thread = key row j of the tile (TMEM lane).
-__device__ __forceinline__ bool fb_softmax(const FbArgs &a, uint8_t *smem, FbBars *bars, uint32_t tmem, int r, int warp,
-                           int lane) {
-  volatile int *abort = &bars->abort;
-  const int row = (warp & 3) * 32 + lane;
-  const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-  const uint32_t tS = tmem + lane_off + col_s(r), tP = tmem + lane_off + col_dp(r);
-  uint8_t *ds_row = smem + FB_SM_DS + r * DS_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
-  const float c = a.scale_log2;
-  uint32_t sf_par = 0, af_par = 0;
-  int use = 0;
-  bool ok = true;
-  for (int it = 0; ok; ++it) {
-    const int slot = it & 1;
-    if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
-    const int item = bars->item[slot];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
-    if (item < 0) break;
-    const FbItem I = fb_decode(a, item);
-    const TileRange R = fb_range(a, I);
-    const int n = fb_halves(R);
-    const int k0 = I.tile * BN, j = k0 + row;
-    const int *lr = a.lo + size_t(I.b) * a.S_pad;
-    for (int u = r; u < n; u += 2) {
-      const int st = (use + u) % FB_STAGES;
-      const uint32_t st_par = ((use + u) / FB_STAGES) & 1;
-      if (!(ok = mbar_wait(&bars->s_full[r], sf_par, abort))) break;
-      sf_par ^= 1;
-      // the stage's lo / lse2 / delta rows arrived by bulk copy: observe their barrier
-      if (!(ok = mbar_wait(&bars->st_full[st], st_par, abort))) break;
-      tc_fence_after();
-      const uint8_t *stage = smem + FB_SM_ST + st * FB_STAGE_STRIDE;
-      const int *lo_q = reinterpret_cast<const int *>(stage + 2 * QH_BYTES);
-      const float *l2_q = reinterpret_cast<const float *>(stage + 2 * QH_BYTES + RT_BYTES);
-      const float *dl_q = reinterpret_cast<const float *>(stage + 2 * QH_BYTES + 2 * RT_BYTES);
-      const int qb = (R.first + (u >> 1)) * BM + (u & 1) * QH;   // first query of the half
-      // Key j is visible from query qb + q iff lo[qb + q] <= j <= qb + q. lo is
-      // non-decreasing, so the visible q form one range [q_from, q_to): q_from = j - qb,
-      // q_to = the number of q with lo <= j. Whole-visible pairs skip the search.
-      int q_from = 0, q_to = QH;
-      if (!(lr[qb + QH - 1] <= k0 && k0 + BN - 1 <= qb)) {
-        q_from = j - qb;
-        int lo_i = 0, hi_i = QH;
-        while (lo_i < hi_i) {
-          const int m = (lo_i + hi_i) >> 1;
-          if (lo_q[m] <= j) lo_i = m + 1; else hi_i = m;
-        }
-        q_to = lo_i;
-      }
-      // 16 queries at a time: their S^T / dP^T columns, row terms and results stay in
-      // registers together
-#pragma unroll 1
-      for (int ch = 0; ch < QH / 16; ++ch) {
-        uint32_t sv[16], dv[16];
-        tmem_ld16(tS + ch * 16, sv);
-        tmem_ld16(tP + ch * 16, dv);
-        tmem_ld_wait();
-        uint32_t pk[8], dk[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float pp[2], dd[2];
-#pragma unroll
-          for (int w = 0; w < 2; ++w) {
-            const int q = ch * 16 + 2 * e + w;
-            float p = ex2_approx(fmaf(__uint_as_float(sv[2 * e + w]), c, -l2_q[q]));
-            if (q < q_from || q >= q_to) p = 0.f;
-            pp[w] = p;
-            dd[w] = p * (__uint_as_float(dv[2 * e + w]) - dl_q[q]);
-          }
-          pk[e] = pack_bf16x2(pp[0], pp[1]);
-          dk[e] = pack_bf16x2(dd[0], dd[1]);
-        }
-        // bf16 results over the 16 columns just read: P^T block, then dS^T block
-        tmem_st8(tS + ch * 16, pk);
-        tmem_st8(tS + ch * 16 + 8, dk);
-        // dS^T row of this key into the 128B-swizzled staging tile: 16-byte chunk
-        // c (queries 8c .. 8c+7) sits at chunk position c ^ (row & 7)
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int chunk = ch * 2 + cc;
-          *reinterpret_cast<uint4 *>(ds_row + ((chunk ^ (row & 7)) << 4)) =
-              make_uint4(dk[4 * cc], dk[4 * cc + 1], dk[4 * cc + 2], dk[4 * cc + 3]);
-        }
-      }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[r]);
-    }
-    if (!ok) break;
-    use += n;
-    // epilogue: region 0's warpgroup writes dV, region 1's writes dK (scaled by 1/sqrt(D))
-    __nv_bfloat16 *dst = (r == 0 ? a.dv : a.dk) + ((size_t(I.b) * a.S + j) * a.H + I.h) * HD;
-    if (n > 0) {
-      if (!(ok = mbar_wait(&bars->acc_full, af_par, abort))) break;
-      af_par ^= 1;
-      tc_fence_after();
-      const uint32_t t_acc = tmem + lane_off + (r == 0 ? COL_DV : COL_DK);
-      const float f = r == 0 ? 1.f : a.inv_sqrt_d;
-      for (int cc = 0; cc < HD; cc += 32) {
-        uint32_t o[32];
-        tmem_ld32(t_acc + cc, o);
-        tmem_ld_wait();
-        uint4 w4[4];
-        uint32_t *wp = reinterpret_cast<uint32_t *>(w4);
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          wp[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * f, __uint_as_float(o[2 * e + 1]) * f);
-        if (j < a.S) {
-          uint4 *d = reinterpret_cast<uint4 *>(dst + cc);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) d[e] = w4[e];
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->acc_empty);
-    } else if (j < a.S) {
-      uint4 *d = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-      for (int e = 0; e < HD / 8; ++e) d[e] = make_uint4(0, 0, 0, 0);
-    }
-  }
-  return ok;
 }
 
 // Tensor bulk reduce-add of a shared-memory box into the fp32 dQ accumulator (the
@@ -445,17 +168,181 @@ __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk
 // Waits until every committed bulk group has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// dQ readout: warp w takes TMEM lanes 32 (w % 4) .. + 31 = head dims 32 (w % 4) .. + 31
-// of dQ^T, and passes every 16-query block of them through one of its two shared
-// staging buffers ([query][dim]) to a tensor bulk reduce-add into the accumulator.
-__device__ __forceinline__ bool fb_readout(const CUtensorMap *tdq, const FbArgs &a, uint8_t *smem, FbBars *bars,
-                                           uint32_t tmem, int warp, int lane) {
+__device__ bool fb_wait_plain(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+  return true;
+}
+
+__device__ __forceinline__ void fb_load_tile(const CUtensorMap *m, uint64_t *bar, uint8_t *dst, int h, int row0,
+                                             int b) {
+  tma_load_4d(m, bar, dst, 0, h, row0, b);
+  tma_load_4d(m, bar, dst + HALF_BYTES, 64, h, row0, b);
+}
+
+// ----------------------------------------------------------------------------- producer
+__device__ __forceinline__ bool fb_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
+                                            const CUtensorMap *tdo, const FbArgs &a, uint8_t *smem, FbBars *bars) {
+  volatile int *abort = &bars->abort;
+  int q_fill = 0, do_fill = 0, own = 0;
+  bool ok = true;
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_empty[slot], ((it >> 1) & 1) ^ 1, abort))) break;
+    const int t = atomicAdd(a.hdr + HDR_TICKET_FUSED, 1);
+    const int item = t < a.n_items ? t : -1;
+    bars->item[slot] = item;
+    mbar_arrive(&bars->item_full[slot]);
+    if (item < 0) break;
+    const FbItem I = fb_decode(a, item);
+    const TileRange R = fb_range(a, I);
+    const int n = fb_tiles(R);
+    if (!(ok = mbar_wait(&bars->own_empty, (it & 1) ^ 1, abort))) break;
+    mbar_arrive_expect_tx(&bars->own_full, 2 * TILE_BYTES);
+    fb_load_tile(tk, &bars->own_full, smem + FB_SM_K, I.h, I.tile * BN, I.b);
+    fb_load_tile(tv, &bars->own_full, smem + FB_SM_V, I.h, I.tile * BN, I.b);
+    ++own;
+    const size_t rowbase = (size_t(I.b) * a.H + I.h) * a.S_pad;
+    for (int j = 0; j < n && ok; ++j) {
+      const int row0 = (R.first + j) * BM;
+      const int qs = q_fill & 1;
+      if (!(ok = mbar_wait(&bars->q_empty[qs], ((q_fill >> 1) & 1) ^ 1, abort))) break;
+      mbar_arrive_expect_tx(&bars->q_full[qs], TILE_BYTES + 3 * RT_BYTES);
+      fb_load_tile(tq, &bars->q_full[qs], smem + FB_SM_Q + qs * TILE_BYTES, I.h, row0, I.b);
+      uint8_t *rt = smem + FB_SM_RT + qs * 3 * RT_BYTES;
+      bulk_load(rt, a.lo + size_t(I.b) * a.S_pad + row0, RT_BYTES, &bars->q_full[qs]);
+      bulk_load(rt + RT_BYTES, a.lse2 + rowbase + row0, RT_BYTES, &bars->q_full[qs]);
+      bulk_load(rt + 2 * RT_BYTES, a.delta + rowbase + row0, RT_BYTES, &bars->q_full[qs]);
+      ++q_fill;
+      if (!(ok = mbar_wait(&bars->do_empty, (do_fill & 1) ^ 1, abort))) break;
+      mbar_arrive_expect_tx(&bars->do_full, TILE_BYTES);
+      fb_load_tile(tdo, &bars->do_full, smem + FB_SM_DO, I.h, row0, I.b);
+      ++do_fill;
+    }
+    if (!ok) break;
+  }
+  bars->q_fill = q_fill;
+  bars->do_fill = do_fill;
+  bars->own_issued = own;
+  return ok;
+}
+
+// ----------------------------------------------------------------------------- MMA issuer
+__device__ __forceinline__ bool fb_mma(const FbArgs &a, uint8_t *smem, FbBars *bars, uint32_t tmem, int lane) {
+  volatile int *abort = &bars->abort;
+  const uint32_t k_s = smem_u32(smem + FB_SM_K), v_s = smem_u32(smem + FB_SM_V);
+  const uint32_t q0_s = smem_u32(smem + FB_SM_Q), do_s = smem_u32(smem + FB_SM_DO);
+  const uint32_t ds_s = smem_u32(smem + FB_SM_DS);
+  int q_use = 0, do_use = 0, own = 0;
+  uint32_t pf_par = 0, dsf_par = 0, dqe_par = 0, ae_par = 1;
+  bool dq_pending = false;
+  bool ok = true;
+
+  for (int it = 0; ok; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
+    const int item = bars->item[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+    if (item < 0) break;
+    const FbItem I = fb_decode(a, item);
+    const int n = fb_tiles(fb_range(a, I));
+    if (!(ok = mbar_wait(&bars->own_full, it & 1, abort))) break;
+    ++own;
+    tc_fence_after();
+
+    // S^T(j) into region A (free once the previous tile's dV and dK have been issued:
+    // the tensor core runs them in order), then dP^T(j) into region B, which holds the
+    // previous tile's dQ^T until the softmax warps have taken it out.
+    auto issue_sdp = [&]() -> bool {
+      const int qs = q_use & 1;
+      if (!mbar_wait(&bars->q_full[qs], (q_use >> 1) & 1, abort)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_kmajor(tmem + COL_A, k_s, q0_s + qs * TILE_BYTES);
+        mma_commit(&bars->s_full);
+      }
+      __syncwarp();
+      if (dq_pending) {
+        if (!mbar_wait(&bars->dq_empty, dqe_par, abort)) return false;
+        dqe_par ^= 1;
+        dq_pending = false;
+      }
+      if (!mbar_wait(&bars->do_full, do_use & 1, abort)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_kmajor(tmem + COL_B, v_s, do_s);
+        mma_commit(&bars->dp_full);
+      }
+      __syncwarp();
+      return true;
+    };
+
+    if (n > 0) ok = issue_sdp();
+    for (int j = 0; j < n && ok; ++j) {
+      const int qs = q_use & 1;
+      if (!(ok = mbar_wait(&bars->p_full, pf_par, abort))) break;
+      pf_par ^= 1;
+      if (j == 0) {
+        if (!(ok = mbar_wait(&bars->acc_empty, ae_par, abort))) break;
+        ae_par ^= 1;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        issue_ts(tmem + COL_DV, tmem + COL_A, do_s, j > 0);   // dV += P^T dO
+        mma_commit(&bars->do_empty);
+      }
+      __syncwarp();
+      ++do_use;
+      if (!(ok = mbar_wait(&bars->ds_full, dsf_par, abort))) break;
+      dsf_par ^= 1;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_ts(tmem + COL_DK, tmem + COL_A + 8, q0_s + qs * TILE_BYTES, j > 0);   // dK += dS^T Q
+        mma_commit(&bars->q_empty[qs]);
+        issue_dqt(tmem + COL_B, k_s, ds_s);                                         // dQ^T = K^T dS^T
+        mma_commit(&bars->dq_full);
+      }
+      __syncwarp();
+      ++q_use;
+      dq_pending = true;
+      if (j + 1 < n) ok = issue_sdp();
+    }
+    if (!ok) break;
+    if (lane == 0) {
+      if (n > 0) mma_commit(&bars->acc_full);
+      mma_commit(&bars->own_empty);
+    }
+    __syncwarp();
+  }
+  if (lane == 0) {
+    bars->q_use = q_use;
+    bars->do_use = do_use;
+    bars->own_used = own;
+  }
+  return ok;
+}
+
+// ----------------------------------------------------------------------------- softmax
+// Warpgroup w: thread = key row `row` of the tile (TMEM lane), query columns
+// [64 w, 64 w + 64) of every streamed tile. Per tile: the P phase, the dS phase, then
+// the readout of its columns of dQ^T.
+__device__ __forceinline__ bool fb_softmax(const CUtensorMap *tdq, const FbArgs &a, uint8_t *smem, FbBars *bars,
+                                           uint32_t tmem, int w, int warp, int lane) {
   volatile int *abort = &bars->abort;
   const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
   const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-  float *stage = reinterpret_cast<float *>(smem + FB_SM_RED + quarter * 2 * RED_BLOCK);
-  uint32_t df_par[2] = {0, 0};
-  int nblk = 0;
+  const uint32_t tA = tmem + lane_off + COL_A + 64 * w;   // this warpgroup's S^T / P^T / dS^T columns
+  const uint32_t tB = tmem + lane_off + COL_B + 64 * w;   // dP^T, then dQ^T
+  // dS^T staging: 64-query half w, row `row` (128 bytes, 16-byte chunks swizzled by row & 7)
+  uint8_t *ds_row = smem + FB_SM_DS + w * (DS_BYTES / 2) + (row >> 3) * 1024 + (row & 7) * 128;
+  float *red = reinterpret_cast<float *>(smem + FB_SM_RED + warp * 2 * RED_BLOCK);
+  const float c = a.scale_log2;
+  const bool red_leader = lane == 0;
+  uint32_t sf_par = 0, dpf_par = 0, dqf_par = 0, af_par = 0;
+  int q_use = 0, nred = 0;
   bool ok = true;
   for (int it = 0; ok; ++it) {
     const int slot = it & 1;
@@ -466,35 +353,161 @@ __device__ __forceinline__ bool fb_readout(const CUtensorMap *tdq, const FbArgs 
     if (item < 0) break;
     const FbItem I = fb_decode(a, item);
     const TileRange R = fb_range(a, I);
-    const int n = fb_halves(R);
-    const int row_bh = (I.b * a.H + I.h) * a.S_pad;   // accumulator row of query 0
-    for (int u = 0; u < n; ++u) {
-      const int r = u & 1;
-      if (!(ok = mbar_wait(&bars->dq_full[r], df_par[r], abort))) break;
-      df_par[r] ^= 1;
+    const int n = fb_tiles(R);
+    const int k0 = I.tile * BN, jk = k0 + row;   // this thread's key
+    const int row_bh = (I.b * a.H + I.h) * a.S_pad;
+    for (int j = 0; j < n; ++j, ++q_use) {
+      const int qs = q_use & 1;
+      const int q0 = (R.first + j) * BM;
+      const uint8_t *rt = smem + FB_SM_RT + qs * 3 * RT_BYTES;
+      const int *lo_q = reinterpret_cast<const int *>(rt);
+      const float4 *l2_q = reinterpret_cast<const float4 *>(rt + RT_BYTES) + 16 * w;
+      const float4 *dl_q = reinterpret_cast<const float4 *>(rt + 2 * RT_BYTES) + 16 * w;
+
+      // ---- P phase: P^T = exp2(S^T c - lse2) on the visible pairs
+      if (!(ok = mbar_wait(&bars->s_full, sf_par, abort))) break;
+      sf_par ^= 1;
+      // the row terms arrived by bulk copy with Q_j: observe that buffer's barrier
+      if (!(ok = mbar_wait(&bars->q_full[qs], (q_use >> 1) & 1, abort))) break;
       tc_fence_after();
-      uint32_t v[QH];
-      tmem_ld32(tmem + lane_off + col_dp(r), v);
-      tmem_ld32(tmem + lane_off + col_dp(r) + 32, v + 32);
+      // Key jk is visible from query q0 + q iff lo[q0 + q] <= jk <= q0 + q; lo is
+      // non-decreasing, so these q form one range [q_from, q_to).
+      int q_from = 0, q_to = BM;
+      if (!(lo_q[BM - 1] <= k0 && k0 + BN - 1 <= q0)) {
+        q_from = jk - q0;
+        int lo_i = 0, hi_i = BM;
+        while (lo_i < hi_i) {
+          const int m = (lo_i + hi_i) >> 1;
+          if (lo_q[m] <= jk) lo_i = m + 1; else hi_i = m;
+        }
+        q_to = lo_i;
+      }
+      q_from -= 64 * w;   // relative to this warpgroup's first column
+      q_to -= 64 * w;
+      float p[64];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sv[16];
+        tmem_ld16(tA + ch * 16, sv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const float4 l2 = l2_q[ch * 4 + e4];
+          const float l2v[4] = {l2.x, l2.y, l2.z, l2.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int q = ch * 16 + e4 * 4 + e;
+            float pv = ex2_approx(fmaf(__uint_as_float(sv[e4 * 4 + e]), c, -l2v[e]));
+            if (q < q_from || q >= q_to) pv = 0.f;
+            p[q] = pv;
+          }
+        }
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(p[ch * 16 + 2 * e], p[ch * 16 + 2 * e + 1]);
+        tmem_st8(tA + ch * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full);
+
+      // ---- dS phase: dS^T = P^T (dP^T - delta) -> TMEM (for dK) and shared memory (for dQ)
+      if (!(ok = mbar_wait(&bars->dp_full, dpf_par, abort))) break;
+      dpf_par ^= 1;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t dv[16];
+        tmem_ld16(tB + ch * 16, dv);
+        tmem_ld_wait();
+        float ds[16];
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const float4 dl = dl_q[ch * 4 + e4];
+          const float dlv[4] = {dl.x, dl.y, dl.z, dl.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            ds[e4 * 4 + e] = p[ch * 16 + e4 * 4 + e] * (__uint_as_float(dv[e4 * 4 + e]) - dlv[e]);
+        }
+        uint32_t dk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dk[e] = pack_bf16x2(ds[2 * e], ds[2 * e + 1]);
+        tmem_st8(tA + ch * 16 + 8, dk);
+        // 16-byte chunks 2 ch and 2 ch + 1 of this key's row (queries 16 ch .. 16 ch + 15)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int chunk = ch * 2 + cc;
+          *reinterpret_cast<uint4 *>(ds_row + ((chunk ^ (row & 7)) << 4)) =
+              make_uint4(dk[4 * cc], dk[4 * cc + 1], dk[4 * cc + 2], dk[4 * cc + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ds_full);
+
+      // ---- dQ readout: this warpgroup's 64 query columns of dQ^T; lane = head dim
+      if (!(ok = mbar_wait(&bars->dq_full, dqf_par, abort))) break;
+      dqf_par ^= 1;
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld32(tB, v);
+      tmem_ld32(tB + 32, v + 32);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->dq_empty[r]);
-      const int row0 = row_bh + (R.first + (u >> 1)) * BM + r * QH;
+      if (lane == 0) mbar_arrive(&bars->dq_empty);
+      const int yq = row_bh + q0 + 64 * w;   // accumulator row of this warpgroup's first query
 #pragma unroll
-      for (int blk = 0; blk < QH / RED_Q; ++blk, ++nblk) {
-        float *buf = stage + (nblk & 1) * (RED_BLOCK / 4);
-        if (lane == 0) bulk_wait_read_1();   // this buffer's previous block has been read
+      for (int blk = 0; blk < 64 / RED_Q; ++blk, ++nred) {
+        float *buf = red + (nred & 1) * (RED_BLOCK / 4);
+        if (red_leader) bulk_wait_read_1();   // this buffer's previous block has been read
         __syncwarp();
 #pragma unroll
         for (int q = 0; q < RED_Q; ++q) buf[q * 32 + lane] = __uint_as_float(v[blk * RED_Q + q]);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) tma_reduce_add_2d(tdq, buf, quarter * 32, row0 + blk * RED_Q);
+        if (red_leader) tma_reduce_add_2d(tdq, buf, quarter * 32, yq + blk * RED_Q);
       }
     }
+    if (!ok) break;
+
+    // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (scaled by 1/sqrt(D))
+    __nv_bfloat16 *dst = (w == 0 ? a.dv : a.dk) + ((size_t(I.b) * a.S + jk) * a.H + I.h) * HD;
+    if (n > 0) {
+      if (!(ok = mbar_wait(&bars->acc_full, af_par, abort))) break;
+      af_par ^= 1;
+      tc_fence_after();
+      const uint32_t t_acc = tmem + lane_off + (w == 0 ? COL_DV : COL_DK);
+      const float f = w == 0 ? 1.f : a.inv_sqrt_d;
+#pragma unroll 1
+      for (int cc = 0; cc < HD; cc += 32) {
+        uint32_t o[32];
+        tmem_ld32(t_acc + cc, o);
+        tmem_ld_wait();
+        uint4 w4[4];
+        uint32_t *wp = reinterpret_cast<uint32_t *>(w4);
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          wp[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * f, __uint_as_float(o[2 * e + 1]) * f);
+        if (jk < a.S) {
+          uint4 *d = reinterpret_cast<uint4 *>(dst + cc);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) d[e] = w4[e];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->acc_empty);
+    } else if (jk < a.S) {
+      uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+      for (int e = 0; e < HD / 8; ++e) d[e] = make_uint4(0, 0, 0, 0);
+    }
   }
-  if (lane == 0) bulk_wait_all();
+  if (red_leader) bulk_wait_all();
   __syncwarp();
   return ok;
 }
@@ -511,8 +524,8 @@ __device__ __forceinline__ void fb_finish(bool ok, const FbArgs &a, FbBars *bars
   __syncthreads();
   if (bars->abort) {
     if (warp == FB_PRODUCER && lane == 0) {
-      for (int k = bars->use; k < bars->fill; ++k)
-        fb_wait_plain(&bars->st_full[k % FB_STAGES], (k / FB_STAGES) & 1);
+      for (int k = bars->q_use; k < bars->q_fill; ++k) fb_wait_plain(&bars->q_full[k & 1], (k >> 1) & 1);
+      for (int k = bars->do_use; k < bars->do_fill; ++k) fb_wait_plain(&bars->do_full, k & 1);
       if (bars->own_issued > bars->own_used) fb_wait_plain(&bars->own_full, (bars->own_issued - 1) & 1);
     }
     if (warp == FB_MMA && lane == 0) {
@@ -545,25 +558,27 @@ __global__ void __launch_bounds__(FB_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < FB_STAGES; ++s) {
-      mbar_init(&bars->st_full[s], 1);
-      mbar_init(&bars->st_empty[s], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+      mbar_init(&bars->item_full[s], 1);
+      mbar_init(&bars->item_empty[s], 9);   // softmax 8 + MMA 1 warps
     }
+    mbar_init(&bars->do_full, 1);
+    mbar_init(&bars->do_empty, 1);
     mbar_init(&bars->own_full, 1);
     mbar_init(&bars->own_empty, 1);
-    for (int r = 0; r < 2; ++r) {
-      mbar_init(&bars->s_full[r], 1);
-      mbar_init(&bars->p_full[r], 4);
-      mbar_init(&bars->dq_full[r], 1);
-      mbar_init(&bars->dq_empty[r], 4);
-      mbar_init(&bars->item_full[r], 1);
-      mbar_init(&bars->item_empty[r], 13);   // softmax 8 + readout 4 + MMA 1 warps
-    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, 8);
+    mbar_init(&bars->ds_full, 8);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_empty, 8);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
-    bars->fill = bars->use = bars->own_issued = bars->own_used = 0;
+    bars->q_fill = bars->q_use = bars->do_fill = bars->do_use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
   }
   if (warp == FB_MMA) {
@@ -575,27 +590,23 @@ __global__ void __launch_bounds__(FB_THREADS, 1)
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
     tma_prefetch_desc(&tdo);
+    tma_prefetch_desc(&tdq);
   }
-  if (warp == FB_READ0 && lane == 0) tma_prefetch_desc(&tdq);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp < FB_READ0) {
-    fb_finish(fb_softmax(a, smem, bars, tmem, warp >> 2, warp, lane), a, bars, tmem, warp, lane);
-  } else if (warp < FB_PRODUCER) {
-    fb_finish(fb_readout(&tdq, a, smem, bars, tmem, warp, lane), a, bars, tmem, warp, lane);
-  } else {
-    bool ok = true;
-    if (warp == FB_PRODUCER) {
-      if (lane == 0) ok = fb_producer(&tq, &tk, &tv, &tdo, a, smem, bars);
-      __syncwarp();
-    } else if (warp == FB_MMA) {
-      ok = fb_mma(a, smem, bars, tmem, lane);
-    }
-    fb_finish(ok, a, bars, tmem, warp, lane);
+  bool ok = true;
+  if (warp < FB_PRODUCER) {
+    ok = fb_softmax(&tdq, a, smem, bars, tmem, warp >> 2, warp, lane);
+  } else if (warp == FB_PRODUCER) {
+    if (lane == 0) ok = fb_producer(&tq, &tk, &tv, &tdo, a, smem, bars);
+    __syncwarp();
+  } else if (warp == FB_MMA) {
+    ok = fb_mma(a, smem, bars, tmem, lane);
   }
+  fb_finish(ok, a, bars, tmem, warp, lane);
 }
 
 // dq[b, s, h, :] = bf16(dqacc[b, h, s, :] / sqrt(D)); one thread per 8 dims.
@@ -623,9 +634,9 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float4 *__restric
 
 }  // namespace
 
-cudaError_t launch_dkdvq(const CUtensorMap &tq64, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const CUtensorMap &tdo64, const CUtensorMap &tdqacc, void *dq, void *dk, void *dv,
-                         const Problem &p, void *workspace, cudaStream_t stream) {
+cudaError_t launch_dkdvq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
+                         const CUtensorMap &tdqacc, void *dq, void *dk, void *dv, const Problem &p, void *workspace,
+                         cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(dkdvq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FB_SMEM);
@@ -640,7 +651,6 @@ cudaError_t launch_dkdvq(const CUtensorMap &tq64, const CUtensorMap &tk, const C
   a.list = reinterpret_cast<const int *>(base + w.off_list_kv);
   a.delta = reinterpret_cast<const float *>(base + w.off_delta);
   a.lse2 = reinterpret_cast<const float *>(base + w.off_lse2);
-  a.dqacc = reinterpret_cast<float *>(base + w.off_dqacc);
   a.hdr = reinterpret_cast<int *>(base + w.off_hdr);
   a.dk = static_cast<__nv_bfloat16 *>(dk);
   a.dv = static_cast<__nv_bfloat16 *>(dv);
@@ -649,20 +659,22 @@ cudaError_t launch_dkdvq(const CUtensorMap &tq64, const CUtensorMap &tk, const C
   a.H = p.H;
   a.nT = w.nT;
   a.S_pad = w.S_pad;
-  a.n_items = p.B * w.nT * p.H;
+  a.n_list = p.B * w.nT;
+  a.n_items = a.n_list * p.H;
   a.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
   a.inv_sqrt_d = 1.f / sqrtf(float(HD));
-  cudaError_t e = cudaMemsetAsync(a.dqacc, 0, w.dqacc_bytes, stream);
+  float *dqacc = reinterpret_cast<float *>(base + w.off_dqacc);
+  cudaError_t e = cudaMemsetAsync(dqacc, 0, w.dqacc_bytes, stream);
   if (e != cudaSuccess) return e;
   const int grid = a.n_items < p.num_sms ? a.n_items : p.num_sms;
-  dkdvq_kernel<<<grid, FB_THREADS, FB_SMEM, stream>>>(tq64, tk, tv, tdo64, tdqacc, a);
+  dkdvq_kernel<<<grid, FB_THREADS, FB_SMEM, stream>>>(tq, tk, tv, tdo, tdqacc, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long total = (long long)p.B * p.S * p.H * (HD / 8);
   long long blocks = (total + 255) / 256;
   const long long cap = (long long)p.num_sms * 16;
   if (blocks > cap) blocks = cap;
-  dq_convert_kernel<<<int(blocks), 256, 0, stream>>>(reinterpret_cast<const float4 *>(a.dqacc),
+  dq_convert_kernel<<<int(blocks), 256, 0, stream>>>(reinterpret_cast<const float4 *>(dqacc),
                                                       static_cast<uint4 *>(dq), p.B, p.S, p.H, w.S_pad,
                                                       a.inv_sqrt_d);
   return cudaGetLastError();

@@ -25,10 +25,10 @@ cudaError_t launch_dkdv(const CUtensorMap &tq, const CUtensorMap &tk, const CUte
                         void *workspace, cudaStream_t stream);
 
 // tdqacc: the workspace's fp32 dQ accumulator as a 2-D tensor map of
-// [B * H * S_pad rows, 128 dims], boxes of 16 rows x 32 dims, no swizzle.
-cudaError_t launch_dkdvq(const CUtensorMap &tq64, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const CUtensorMap &tdo64, const CUtensorMap &tdqacc, void *dq, void *dk, void *dv,
-                         const Problem &p, void *workspace, cudaStream_t stream);
+// [B * H * S_pad rows, 128 dims], boxes of 8 rows x 32 dims, no swizzle.
+cudaError_t launch_dkdvq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
+                         const CUtensorMap &tdqacc, void *dq, void *dk, void *dv, const Problem &p, void *workspace,
+                         cudaStream_t stream);
 
 cudaError_t launch_dq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                       const CUtensorMap &tdo, void *dq, const Problem &p, void *workspace,
