@@ -378,8 +378,8 @@ def main():
     ap.add_argument("--seq", type=int, default=0, help="custom workload: sequence length (one document)")
     ap.add_argument("--heads", type=int, default=32, help="custom workload: heads")
     ap.add_argument("--batch", type=int, default=1, help="custom workload: batch rows")
-    ap.add_argument("--bwd", choices=["fused", "separate"], default="fused",
-                    help="backward path: one dK/dV/dQ kernel (default) or separate dK/dV and dQ kernels")
+    ap.add_argument("--bwd", choices=["separate", "fused"], default="separate",
+                    help="backward path: dK/dV and dQ kernels (default) or one dK/dV/dQ kernel")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

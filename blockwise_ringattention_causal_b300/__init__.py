@@ -251,20 +251,20 @@ def forward(q, k, v, seg_ids=None, pos=None, kv_chunks=1, workspace=None, stream
     return out, lse, workspace
 
 
-def backward(q, k, v, out, dout, lse, seg_ids=None, pos=None, workspace=None, stream=None, deterministic=False):
+def backward(q, k, v, out, dout, lse, seg_ids=None, pos=None, workspace=None, stream=None, fused=False):
     """Allocate dq/dk/dv and run the backward pass. Returns (dq, dk, dv).
 
-    The default runs lwm_attn_bwd (row-dot pre-pass + single-kernel dK/dV/dQ, dq summed
-    in fp32 in a scheduling-dependent order). ``deterministic=True`` runs the
-    metadata pre-pass and the LWM_BWD_ALL stages (separate dK/dV and dQ kernels,
-    every gradient bitwise reproducible)."""
+    The default runs lwm_attn_bwd (row-dot pre-pass, dK/dV kernel, dQ kernel; every
+    gradient bitwise reproducible). ``fused=True`` runs the metadata pre-pass and the
+    LWM_BWD_DELTA | LWM_BWD_FUSED stages (one dK/dV/dQ kernel, dq summed in fp32 in a
+    scheduling-dependent order)."""
     B, S, H, D = _shape(q)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
         workspace = new_workspace(B, S, H, D, q.device)
-    if deterministic:
+    if fused:
         lwm_attn_prepare(seg_ids, pos, B, S, H, D, 1, workspace, stream)
-        lwm_attn_bwd_stages(q, k, v, out, dout, lse, dq, dk, dv, LWM_BWD_ALL, workspace, stream)
+        lwm_attn_bwd_stages(q, k, v, out, dout, lse, dq, dk, dv, LWM_BWD_DELTA | LWM_BWD_FUSED, workspace, stream)
     else:
         lwm_attn_bwd(q, k, v, out, dout, lse, seg_ids, pos, dq, dk, dv, workspace, stream)
     return dq, dk, dv

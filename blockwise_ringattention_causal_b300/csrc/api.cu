@@ -180,7 +180,7 @@ lwm_status check_bwd_args(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse))
     return LWM_ERR_ALIGNMENT;
-  return check_workspace(ws, ws_bytes, B, S, H, true);
+  return check_workspace(ws, ws_bytes, B, S, H, false);
 }
 
 lwm_status bwd_common(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,
@@ -313,8 +313,7 @@ lwm_status lwm_attn_bwd(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
   DeviceInfo d;
   LWM_TRY(device_info(d));
   LWM_TRY(prepare_impl(seg_ids, pos, B, S, H, 1, workspace, stream));
-  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, LWM_BWD_DELTA | LWM_BWD_FUSED, workspace, stream,
-                    d);
+  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, LWM_BWD_ALL, workspace, stream, d);
 }
 
 lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,
@@ -324,8 +323,7 @@ lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm
   LWM_TRY(check_bwd_args(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, D, workspace, workspace_bytes));
   DeviceInfo d;
   LWM_TRY(device_info(d));
-  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, LWM_BWD_DELTA | LWM_BWD_FUSED, workspace, stream,
-                    d);
+  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, S, H, LWM_BWD_ALL, workspace, stream, d);
 }
 
 lwm_status lwm_attn_bwd_stages(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, const lwm_bf16 *out,

@@ -96,46 +96,17 @@ cudaError_t launch_delta(const void *out, const void *dout, const float *lse, co
 namespace {
 
 // ----------------------------------------------------------------------------- shared pieces
-// Both backward kernels keep one 128-row tile of their "own" rows resident (key rows
-// for dK/dV, query rows for dQ) and stream 128-row tiles of the other side. Each
-// streamed tile is processed as two 64-row halves h = 0, 1, one per softmax
-// warpgroup, so that warpgroup h works on half h while the tensor core computes the
-// other half's products. TMEM columns (fp32):
-//   0-63 S_0 | 64-127 dP_0 | 128-191 S_1 | 192-255 dP_1 | 256-383 acc0 | 384-511 acc1
-// The bf16 operands written back by the softmax warps (P, dS) overwrite the first 32
-// columns of the S / dP block they were computed from.
+// Both kernels keep one 128-row tile of their "own" rows resident (key rows for dK/dV,
+// query rows for dQ) and stream 128-row tiles of the other side; every product is
+// 128 x 128 x 128 (K = 16 per instruction). Warp roles: 0-3 and 4-7 two softmax
+// warpgroups, warpgroup w owning columns [64 w, 64 w + 64) of every 128 x 128 score
+// tile (thread = row of the tile = TMEM lane); 8 TMA producer; 9 MMA issuer; 10-11
+// idle (3 warps per SM sub-partition: up to 168 registers per thread).
 constexpr int BW_WARPS = 12;
 constexpr int BW_THREADS = BW_WARPS * 32;
 constexpr int BW_PRODUCER = 8;
 constexpr int BW_MMA = 9;
-constexpr int HALF_ROWS = 64;
-constexpr int HALF_ROW_BYTES = HALF_ROWS * 128;   // 64 rows of one 64-dim swizzled box
-constexpr uint32_t COL_ACC0 = 256, COL_ACC1 = 384;
-constexpr uint32_t IDESC_HALF = idesc_bf16(BM, HALF_ROWS, false, false);   // [128 x 64] = A . B_half^T
-constexpr uint32_t IDESC_ACC = idesc_bf16(BM, HD, false, true);            // acc += X(tmem) . Y_half
-
-__device__ __forceinline__ uint32_t col_s(int h) { return uint32_t(h) * 128u; }
-__device__ __forceinline__ uint32_t col_dp(int h) { return uint32_t(h) * 128u + 64u; }
-
-// D[128 x 64] = A[128 rows x 128 dims] . B[64 rows x 128 dims]^T, both K-major tiles
-// (two 64-dim 128B-swizzled boxes, HALF_BYTES apart); `b_half` points at the first of
-// the 64 B rows inside the tile.
-__device__ __forceinline__ void issue_half(uint32_t d_tmem, uint32_t a_s, uint32_t b_half) {
-#pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk) {
-    const uint32_t off = uint32_t(kk >> 2) * HALF_BYTES + uint32_t(kk & 3) * 32;
-    mma_ss(d_tmem, sdesc_sw128(a_s + off, 16, 1024), sdesc_sw128(b_half + off, 16, 1024), IDESC_HALF, kk > 0);
-  }
-}
-
-// acc[128 x 128] (+)= X[128 x 64] (bf16 in TMEM) . Y[64 rows x 128 dims] with Y read
-// MN-major (dims contiguous): 16 rows = two 8-row groups of 1024 bytes.
-__device__ __forceinline__ void issue_acc(uint32_t acc, uint32_t x_tmem, uint32_t y_half, bool accumulate) {
-#pragma unroll
-  for (int kk = 0; kk < HALF_ROWS / 16; ++kk)
-    mma_ts(acc, x_tmem + uint32_t(kk) * 8, sdesc_sw128(y_half + uint32_t(kk) * 2048, HALF_BYTES, 1024), IDESC_ACC,
-           (accumulate || kk > 0) ? 1u : 0u);
-}
+constexpr int RT_BYTES = BM * 4;   // 128 row terms (int32 / fp32)
 
 __device__ __forceinline__ void load_tile(const CUtensorMap *m, uint64_t *bar, uint8_t *dst, int h, int row0, int b) {
   tma_load_4d(m, bar, dst, 0, h, row0, b);
@@ -149,10 +120,10 @@ __device__ bool bounded_wait_plain_bw(uint64_t *bar, uint32_t parity) {
   return true;
 }
 
-// Writes one 128-value fp32 TMEM row (this thread's lane, columns c0..c0+n) scaled by
-// `f` as bf16 to dst (n multiple of 32).
-__device__ __forceinline__ void store_row_bf16(uint32_t t_addr, int n, float f, __nv_bfloat16 *dst, bool valid) {
-  for (int cc = 0; cc < n; cc += 32) {
+// Writes 64 fp32 TMEM columns of this thread's lane, scaled by f, as bf16 to dst.
+__device__ __forceinline__ void store_cols_bf16(uint32_t t_addr, float f, __nv_bfloat16 *dst, bool valid) {
+#pragma unroll 1
+  for (int cc = 0; cc < 64; cc += 32) {
     uint32_t o[32];
     tmem_ld32(t_addr + cc, o);
     tmem_ld_wait();
@@ -168,7 +139,7 @@ __device__ __forceinline__ void store_row_bf16(uint32_t t_addr, int n, float f, 
   }
 }
 
-__device__ __forceinline__ void zero_row_bf16(__nv_bfloat16 *dst, int n) {
+__device__ __forceinline__ void zero_cols_bf16(__nv_bfloat16 *dst, int n) {
   uint4 *d = reinterpret_cast<uint4 *>(dst);
   for (int e = 0; e < n / 8; ++e) d[e] = make_uint4(0, 0, 0, 0);
 }
@@ -176,12 +147,12 @@ __device__ __forceinline__ void zero_row_bf16(__nv_bfloat16 *dst, int n) {
 struct BwArgs {
   const int *lo;       // [B, S_pad]
   const int *kend;     // [B, nT]
-  const int *list;     // work list (b * nT + tile)
+  const int *list;     // (b * nT + tile), longest first
   const float *delta;  // [B, H, S_pad]
   const float *lse2;   // [B, H, S_pad], lse * log2(e), +inf where nothing is visible
   int *hdr;
   __nv_bfloat16 *out0, *out1;   // dK/dV kernel: dv, dk; dQ kernel: dq
-  int B, S, H, nT, S_pad, n_items;
+  int B, S, H, nT, S_pad, n_list, n_items;
   float scale_log2;   // log2(e) / sqrt(D)
   float inv_sqrt_d;
 };
@@ -190,9 +161,11 @@ struct BwItem {
   int b, h, tile;
 };
 
+// Items of one head are consecutive (head-major), each head's tiles longest first, so
+// that the CTAs running at the same time share the streamed tiles in L2.
 __device__ __forceinline__ BwItem bw_decode(const BwArgs &a, int item) {
-  const int e = a.list[item / a.H];
-  return {e / a.nT, item % a.H, e % a.nT};
+  const int e = a.list[item % a.n_list];
+  return {e / a.nT, item / a.n_list, e % a.nT};
 }
 
 // Streamed-tile range of an item: dQ -> key tiles the query tile needs; dK/dV ->
@@ -210,307 +183,28 @@ __device__ __forceinline__ TileRange dkdv_range(const BwArgs &a, const BwItem &I
   }
   return r;
 }
-
-// A tile pair is "full" when every (query, key) pair in it is visible: no masking.
-__device__ __forceinline__ bool pair_full(const int *lo_row, int q0, int k0) {
-  return lo_row[q0 + BM - 1] <= k0 && k0 + BN - 1 <= q0;
-}
-
-// ============================================================================= dQ
-// Item: (b, h, query tile). Resident: Q and dO tiles. Streamed: K_j, V_j tiles.
-//   S_h  = Q . K_h^T,  dP_h = dO . V_h^T            (h = 64-key half of tile j)
-//   P    = exp2(S c - lse2_i) (masked),  dS = P (dP - delta_i)
-//   dQ  += dS_h . K_h          (acc0; scaled by 1/sqrt(D) in the epilogue)
-constexpr int DQ_STAGES = 2;
-constexpr int DQ_SM_Q = 0, DQ_SM_DO = TILE_BYTES, DQ_SM_KV = 2 * TILE_BYTES;
-constexpr int DQ_SM_BAR = DQ_SM_KV + DQ_STAGES * 2 * TILE_BYTES;
-
-struct DqBars {
-  uint64_t kv_full[DQ_STAGES], kv_empty[DQ_STAGES];
-  uint64_t own_full, own_empty;
-  uint64_t s_full[2], p_full[2];
-  uint64_t acc_full, acc_empty;
-  uint64_t item_full[2], item_empty[2];
-  uint64_t drain;
-  int item[2];
-  uint32_t tmem_base;
-  int abort;
-  int fill, use, own_issued, own_used;
-};
-constexpr int DQ_SMEM = DQ_SM_BAR + int(sizeof(DqBars)) + 1024;
-
-__global__ void __launch_bounds__(BW_THREADS, 1)
-    dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const BwArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  DqBars *bars = reinterpret_cast<DqBars *>(smem + DQ_SM_BAR);
-  volatile int *abort = &bars->abort;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < DQ_STAGES; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
-    }
-    mbar_init(&bars->own_full, 1);
-    mbar_init(&bars->own_empty, 1);
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(&bars->s_full[h], 1);
-      mbar_init(&bars->p_full[h], 4);
-      mbar_init(&bars->item_full[h], 1);
-      mbar_init(&bars->item_empty[h], 9);
-    }
-    mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, 8);
-    mbar_init(&bars->drain, 1);
-    bars->abort = 0;
-    bars->fill = bars->use = bars->own_issued = bars->own_used = 0;
-    fence_mbar_init();
-  }
-  if (warp == BW_MMA) {
-    tmem_alloc(&bars->tmem_base, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
-  bool ok = true;
-
-  if (warp == BW_PRODUCER) {
-    if (lane == 0) {
-      int fill = 0, own = 0;
-      for (int it = 0;; ++it) {
-        const int slot = it & 1;
-        if (!(ok = mbar_wait(&bars->item_empty[slot], ((it >> 1) & 1) ^ 1, abort))) break;
-        const int t = atomicAdd(a.hdr + HDR_TICKET_DQ, 1);
-        const int item = t < a.n_items ? t : -1;
-        bars->item[slot] = item;
-        mbar_arrive(&bars->item_full[slot]);
-        if (item < 0) break;
-        const BwItem I = bw_decode(a, item);
-        const TileRange R = dq_range(a, I);
-        if (!(ok = mbar_wait(&bars->own_empty, (it & 1) ^ 1, abort))) break;
-        mbar_arrive_expect_tx(&bars->own_full, 2 * TILE_BYTES);
-        load_tile(&tq, &bars->own_full, smem + DQ_SM_Q, I.h, I.tile * BM, I.b);
-        load_tile(&tdo, &bars->own_full, smem + DQ_SM_DO, I.h, I.tile * BM, I.b);
-        ++own;
-        for (int j = R.first; j <= R.last && ok; ++j) {
-          const int st = fill % DQ_STAGES;
-          if (!(ok = mbar_wait(&bars->kv_empty[st], ((fill / DQ_STAGES) & 1) ^ 1, abort))) break;
-          mbar_arrive_expect_tx(&bars->kv_full[st], 2 * TILE_BYTES);
-          uint8_t *dst = smem + DQ_SM_KV + st * 2 * TILE_BYTES;
-          load_tile(&tk, &bars->kv_full[st], dst, I.h, j * BN, I.b);
-          load_tile(&tv, &bars->kv_full[st], dst + TILE_BYTES, I.h, j * BN, I.b);
-          ++fill;
-        }
-        if (!ok) break;
-      }
-      bars->fill = fill;
-      bars->own_issued = own;
-    }
-    __syncwarp();
-  } else if (warp == BW_MMA) {
-    const uint32_t q_s = smem_u32(smem + DQ_SM_Q), do_s = smem_u32(smem + DQ_SM_DO);
-    const uint32_t kv0 = smem_u32(smem + DQ_SM_KV);
-    int use = 0, own = 0;
-    uint32_t pf_par[2] = {0, 0}, ae_par = 1;
-    for (int it = 0; ok; ++it) {
-      const int slot = it & 1;
-      if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
-      const int item = bars->item[slot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
-      if (item < 0) break;
-      const BwItem I = bw_decode(a, item);
-      const TileRange R = dq_range(a, I);
-      if (!(ok = mbar_wait(&bars->own_full, it & 1, abort))) break;
-      ++own;
-      tc_fence_after();
-      bool first = true;
-      if (!R.empty()) {
-        // prologue: S and dP of both halves of the first key tile
-        int st = use % DQ_STAGES;
-        if (!(ok = mbar_wait(&bars->kv_full[st], (use / DQ_STAGES) & 1, abort))) break;
-        ++use;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t k_s = kv0 + st * 2 * TILE_BYTES, v_s = k_s + TILE_BYTES;
-          for (int h = 0; h < 2; ++h) {
-            issue_half(tmem + col_s(h), q_s, k_s + h * HALF_ROW_BYTES);
-            issue_half(tmem + col_dp(h), do_s, v_s + h * HALF_ROW_BYTES);
-            mma_commit(&bars->s_full[h]);
-          }
-        }
-        __syncwarp();
-        for (int j = R.first; j <= R.last && ok; ++j) {
-          const bool has_next = j < R.last;
-          const uint32_t k_s = kv0 + st * 2 * TILE_BYTES;
-          int st2 = -1;
-          if (first) {
-            if (!(ok = mbar_wait(&bars->acc_empty, ae_par, abort))) break;
-            ae_par ^= 1;
-          }
-          for (int h = 0; h < 2 && ok; ++h) {
-            if (!(ok = mbar_wait(&bars->p_full[h], pf_par[h], abort))) break;
-            pf_par[h] ^= 1;
-            tc_fence_after();
-            if (lane == 0) issue_acc(tmem + COL_ACC0, tmem + col_s(h), k_s + h * HALF_ROW_BYTES, !first);
-            first = false;
-            if (h == 1 && lane == 0) mma_commit(&bars->kv_empty[st]);
-            if (has_next) {
-              if (h == 0) {
-                st2 = use % DQ_STAGES;
-                if (!(ok = mbar_wait(&bars->kv_full[st2], (use / DQ_STAGES) & 1, abort))) break;
-                ++use;
-                tc_fence_after();
-              }
-              if (lane == 0) {
-                const uint32_t k2 = kv0 + st2 * 2 * TILE_BYTES, v2 = k2 + TILE_BYTES;
-                issue_half(tmem + col_s(h), q_s, k2 + h * HALF_ROW_BYTES);
-                issue_half(tmem + col_dp(h), do_s, v2 + h * HALF_ROW_BYTES);
-                mma_commit(&bars->s_full[h]);
-              }
-            }
-          }
-          __syncwarp();
-          st = st2;
-        }
-        if (!ok) break;
-      }
-      if (lane == 0) {
-        mma_commit(&bars->own_empty);
-        if (!first) mma_commit(&bars->acc_full);
-      }
-      __syncwarp();
-    }
-    if (lane == 0) {
-      bars->use = use;
-      bars->own_used = own;
-    }
-  } else if (warp < 8) {
-    const int h = warp >> 2;   // key half this warpgroup owns
-    const int r = (warp & 3) * 32 + lane;
-    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_off + col_s(h), tP = tmem + lane_off + col_dp(h);
-    const float c = a.scale_log2;
-    uint32_t sf_par = 0, af_par = 0;
-    for (int it = 0; ok; ++it) {
-      const int slot = it & 1;
-      if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
-      const int item = bars->item[slot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
-      if (item < 0) break;
-      const BwItem I = bw_decode(a, item);
-      const TileRange R = dq_range(a, I);
-      const int q0 = I.tile * BM, i = q0 + r;
-      const int *lr = a.lo + size_t(I.b) * a.S_pad;
-      const int lo_i = lr[i];
-      const size_t rowterm = (size_t(I.b) * a.H + I.h) * a.S_pad + i;
-      const float l2 = a.lse2[rowterm], dl = a.delta[rowterm];
-      for (int j = R.first; j <= R.last; ++j) {
-        if (!(ok = mbar_wait(&bars->s_full[h], sf_par, abort))) break;
-        sf_par ^= 1;
-        tc_fence_after();
-        const int k0 = j * BN;
-        const bool full = pair_full(lr, q0, k0);
-        const int kb = k0 + h * HALF_ROWS;   // first key of this half
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(tS + ch * 32, sv);
-          tmem_ld32(tP + ch * 32, dv);
-          tmem_ld_wait();
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float ds2[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int cidx = 2 * e + u;
-              float p = ex2_approx(fmaf(__uint_as_float(sv[cidx]), c, -l2));
-              if (!full) {
-                const int kj = kb + ch * 32 + cidx;
-                if (kj < lo_i || kj > i) p = 0.f;
-              }
-              ds2[u] = p * (__uint_as_float(dv[cidx]) - dl);
-            }
-            pk[e] = pack_bf16x2(ds2[0], ds2[1]);
-          }
-          tmem_st16(tS + ch * 16, pk);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_full[h]);
-      }
-      if (!ok) break;
-      __nv_bfloat16 *dst = a.out0 + ((size_t(I.b) * a.S + i) * a.H + I.h) * HD + h * 64;
-      if (!R.empty()) {
-        if (!(ok = mbar_wait(&bars->acc_full, af_par, abort))) break;
-        af_par ^= 1;
-        tc_fence_after();
-        store_row_bf16(tmem + lane_off + COL_ACC0 + h * 64, 64, a.inv_sqrt_d, dst, i < a.S);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->acc_empty);
-      } else if (i < a.S) {
-        zero_row_bf16(dst, 64);
-      }
-    }
-  }
-
-  if (!ok) {
-    bars->abort = 1;
-    raise_error(a.hdr + HDR_ERR, ERRBIT_TIMEOUT);
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (bars->abort) {
-    if (warp == BW_PRODUCER && lane == 0) {
-      for (int n = bars->use; n < bars->fill; ++n)
-        bounded_wait_plain_bw(&bars->kv_full[n % DQ_STAGES], (n / DQ_STAGES) & 1);
-      if (bars->own_issued > bars->own_used) bounded_wait_plain_bw(&bars->own_full, (bars->own_issued - 1) & 1);
-    }
-    if (warp == BW_MMA && lane == 0) {
-      mma_commit(&bars->drain);
-      bounded_wait_plain_bw(&bars->drain, 0);
-    }
-    __syncthreads();
-  }
-  if (warp == BW_MMA) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(a.hdr + HDR_DONE_DQ, 1) == int(gridDim.x) - 1) {
-      a.hdr[HDR_TICKET_DQ] = 0;
-      a.hdr[HDR_DONE_DQ] = 0;
-      __threadfence();
-    }
-  }
-}
+__device__ __forceinline__ int range_tiles(const TileRange &R) { return R.empty() ? 0 : R.last - R.first + 1; }
 
 // ============================================================================= dK/dV
-// Item: (b, h, key tile). Resident: K and V tiles. Streamed: Q_i, dO_i tiles plus the
-// tile's lo / lse2 / delta rows (bulk copies). Per 64-query half h of tile i:
-//   S^T_h = K . Q_h^T,  dP^T_h = V . dO_h^T       (rows = keys, columns = queries)
-//   P^T = exp2(S^T c - lse2) (masked), dS^T = P^T (dP^T - delta)
-//   dV += P^T_h . dO_h (acc0),  dK += dS^T_h . Q_h (acc1; scaled by 1/sqrt(D) at the end)
-constexpr int KV_STAGES_BW = 2;
-constexpr int ROWTERM_BYTES = BM * 4;   // 128 fp32 / int32 values
+// Item: (b, h, key tile). Resident: K and V. Streamed: Q_j, dO_j and the rows' lo /
+// lse2 / delta terms (two stages). Per query tile j:
+//   S^T  = K . Q_j^T  -> A           dP^T = V . dO_j^T -> B
+//   P^T  = exp2(S^T c - lse2) (masked)        -> bf16 over A (columns 16c .. 16c+7 of chunk c)
+//   dS^T = P^T (dP^T - delta)                 -> bf16 over B (the same columns of B)
+//   dV  += P^T . dO_j,  dK += dS^T . Q_j      (dK scaled by 1/sqrt(D) in the epilogue)
+// TMEM: A [0, 128), B [128, 256), dV [256, 384), dK [384, 512). Tensor-core order per
+// tile: dV(j), S^T(j+1), dK(j), dP^T(j+1), so that the P phase of tile j+1 runs under
+// dK(j) and dP^T(j+1), and the dS phase of tile j under dV(j) and S^T(j+1).
+constexpr int KV_STAGE_BYTES = 2 * TILE_BYTES + 3 * RT_BYTES;   // Q, dO, lo, lse2, delta
+constexpr int KV_STAGE_STRIDE = (KV_STAGE_BYTES + 1023) & ~1023;
 constexpr int KVB_SM_K = 0, KVB_SM_V = TILE_BYTES, KVB_SM_ST = 2 * TILE_BYTES;
-constexpr int KVB_STAGE_BYTES = 2 * TILE_BYTES + 3 * ROWTERM_BYTES;   // Q, dO, lo, lse2, delta
-constexpr int KVB_SM_BAR = KVB_SM_ST + KV_STAGES_BW * ((KVB_STAGE_BYTES + 1023) & ~1023);
-constexpr int KVB_STAGE_STRIDE = (KVB_STAGE_BYTES + 1023) & ~1023;
+constexpr int KVB_SM_BAR = KVB_SM_ST + 2 * KV_STAGE_STRIDE;
+constexpr uint32_t KV_COL_A = 0, KV_COL_B = 128, KV_COL_DV = 256, KV_COL_DK = 384;
 
 struct KvbBars {
-  uint64_t st_full[KV_STAGES_BW], st_empty[KV_STAGES_BW];
+  uint64_t st_full[2], st_empty[2];
   uint64_t own_full, own_empty;
-  uint64_t s_full[2], p_full[2];
+  uint64_t s_full, dp_full, p_full, ds_full;
   uint64_t acc_full, acc_empty;
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
@@ -520,6 +214,267 @@ struct KvbBars {
   int fill, use, own_issued, own_used;
 };
 constexpr int KVB_SMEM = KVB_SM_BAR + int(sizeof(KvbBars)) + 1024;
+static_assert(KVB_SMEM <= 232448, "shared memory budget of one CTA");
+
+__device__ __forceinline__ bool kv_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
+                                            const CUtensorMap *tdo, const BwArgs &a, uint8_t *smem, KvbBars *bars) {
+  volatile int *abort = &bars->abort;
+  int fill = 0, own = 0;
+  bool ok = true;
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_empty[slot], ((it >> 1) & 1) ^ 1, abort))) break;
+    const int t = atomicAdd(a.hdr + HDR_TICKET_DKDV, 1);
+    const int item = t < a.n_items ? t : -1;
+    bars->item[slot] = item;
+    mbar_arrive(&bars->item_full[slot]);
+    if (item < 0) break;
+    const BwItem I = bw_decode(a, item);
+    const TileRange R = dkdv_range(a, I);
+    const int n = range_tiles(R);
+    if (!(ok = mbar_wait(&bars->own_empty, (it & 1) ^ 1, abort))) break;
+    mbar_arrive_expect_tx(&bars->own_full, 2 * TILE_BYTES);
+    load_tile(tk, &bars->own_full, smem + KVB_SM_K, I.h, I.tile * BN, I.b);
+    load_tile(tv, &bars->own_full, smem + KVB_SM_V, I.h, I.tile * BN, I.b);
+    ++own;
+    const size_t rowbase = (size_t(I.b) * a.H + I.h) * a.S_pad;
+    for (int j = 0; j < n && ok; ++j) {
+      const int st = fill & 1;
+      if (!(ok = mbar_wait(&bars->st_empty[st], ((fill >> 1) & 1) ^ 1, abort))) break;
+      mbar_arrive_expect_tx(&bars->st_full[st], KV_STAGE_BYTES);
+      uint8_t *dst = smem + KVB_SM_ST + st * KV_STAGE_STRIDE;
+      const int row0 = (R.first + j) * BM;
+      load_tile(tq, &bars->st_full[st], dst, I.h, row0, I.b);
+      load_tile(tdo, &bars->st_full[st], dst + TILE_BYTES, I.h, row0, I.b);
+      bulk_load(dst + 2 * TILE_BYTES, a.lo + size_t(I.b) * a.S_pad + row0, RT_BYTES, &bars->st_full[st]);
+      bulk_load(dst + 2 * TILE_BYTES + RT_BYTES, a.lse2 + rowbase + row0, RT_BYTES, &bars->st_full[st]);
+      bulk_load(dst + 2 * TILE_BYTES + 2 * RT_BYTES, a.delta + rowbase + row0, RT_BYTES, &bars->st_full[st]);
+      ++fill;
+    }
+    if (!ok) break;
+  }
+  bars->fill = fill;
+  bars->own_issued = own;
+  return ok;
+}
+
+__device__ __forceinline__ bool kv_mma(const BwArgs &a, uint8_t *smem, KvbBars *bars, uint32_t tmem, int lane) {
+  volatile int *abort = &bars->abort;
+  const uint32_t k_s = smem_u32(smem + KVB_SM_K), v_s = smem_u32(smem + KVB_SM_V);
+  const uint32_t st0 = smem_u32(smem + KVB_SM_ST);
+  int use = 0, own = 0;
+  uint32_t pf_par = 0, dsf_par = 0, ae_par = 1;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
+    const int item = bars->item[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+    if (item < 0) break;
+    const BwItem I = bw_decode(a, item);
+    const int n = range_tiles(dkdv_range(a, I));
+    if (!(ok = mbar_wait(&bars->own_full, it & 1, abort))) break;
+    ++own;
+    tc_fence_after();
+    const int base = use;
+    auto q_s = [&](int j) { return st0 + uint32_t((base + j) & 1) * KV_STAGE_STRIDE; };
+    auto wait_stage = [&](int j) -> bool {
+      if (!mbar_wait(&bars->st_full[(base + j) & 1], ((base + j) >> 1) & 1, abort)) return false;
+      tc_fence_after();
+      return true;
+    };
+    if (n > 0) {
+      if (!(ok = wait_stage(0))) break;
+      if (lane == 0) {
+        mma_tile_kk(tmem + KV_COL_A, k_s, q_s(0), false);              // S^T(0) = K Q^T
+        mma_commit(&bars->s_full);
+        mma_tile_kk(tmem + KV_COL_B, v_s, q_s(0) + TILE_BYTES, false); // dP^T(0) = V dO^T
+        mma_commit(&bars->dp_full);
+      }
+      __syncwarp();
+    }
+    for (int j = 0; j < n && ok; ++j) {
+      if (!(ok = mbar_wait(&bars->p_full, pf_par, abort))) break;
+      pf_par ^= 1;
+      if (j == 0) {
+        if (!(ok = mbar_wait(&bars->acc_empty, ae_par, abort))) break;
+        ae_par ^= 1;
+      }
+      tc_fence_after();
+      if (lane == 0) mma_tile_ts(tmem + KV_COL_DV, tmem + KV_COL_A, q_s(j) + TILE_BYTES, j > 0);   // dV += P^T dO
+      __syncwarp();
+      const bool more = j + 1 < n;
+      if (more) {
+        if (!(ok = wait_stage(j + 1))) break;
+        if (lane == 0) {
+          mma_tile_kk(tmem + KV_COL_A, k_s, q_s(j + 1), false);   // S^T(j+1): A is free after dV(j) in order
+          mma_commit(&bars->s_full);
+        }
+        __syncwarp();
+      }
+      if (!(ok = mbar_wait(&bars->ds_full, dsf_par, abort))) break;
+      dsf_par ^= 1;
+      tc_fence_after();
+      if (lane == 0) {
+        mma_tile_ts(tmem + KV_COL_DK, tmem + KV_COL_B, q_s(j), j > 0);   // dK += dS^T Q
+        mma_commit(&bars->st_empty[(base + j) & 1]);
+        if (more) {
+          mma_tile_kk(tmem + KV_COL_B, v_s, q_s(j + 1) + TILE_BYTES, false);   // dP^T(j+1)
+          mma_commit(&bars->dp_full);
+        }
+      }
+      __syncwarp();
+    }
+    if (!ok) break;
+    use = base + n;
+    if (lane == 0) {
+      if (n > 0) mma_commit(&bars->acc_full);
+      mma_commit(&bars->own_empty);
+    }
+    __syncwarp();
+  }
+  if (lane == 0) {
+    bars->use = use;
+    bars->own_used = own;
+  }
+  return ok;
+}
+
+// Softmax warpgroup w of the dK/dV kernel: thread = key row `row`; query columns
+// [64 w, 64 w + 64) of every streamed tile.
+__device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBars *bars, uint32_t tmem, int w,
+                                           int warp, int lane) {
+  volatile int *abort = &bars->abort;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+  const uint32_t tA = tmem + lane_off + KV_COL_A + 64 * w;
+  const uint32_t tB = tmem + lane_off + KV_COL_B + 64 * w;
+  const float c = a.scale_log2;
+  uint32_t sf_par = 0, dpf_par = 0, af_par = 0;
+  int use = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
+    const int item = bars->item[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+    if (item < 0) break;
+    const BwItem I = bw_decode(a, item);
+    const TileRange R = dkdv_range(a, I);
+    const int n = range_tiles(R);
+    const int k0 = I.tile * BN, jk = k0 + row;   // this thread's key
+    for (int j = 0; j < n; ++j, ++use) {
+      const int st = use & 1;
+      const uint8_t *stage = smem + KVB_SM_ST + st * KV_STAGE_STRIDE;
+      const int *lo_q = reinterpret_cast<const int *>(stage + 2 * TILE_BYTES);
+      const float4 *l2_q = reinterpret_cast<const float4 *>(stage + 2 * TILE_BYTES + RT_BYTES) + 16 * w;
+      const float4 *dl_q = reinterpret_cast<const float4 *>(stage + 2 * TILE_BYTES + 2 * RT_BYTES) + 16 * w;
+      const int q0 = (R.first + j) * BM;
+
+      // ---- P phase
+      if (!(ok = mbar_wait(&bars->s_full, sf_par, abort))) break;
+      sf_par ^= 1;
+      // the stage's row terms arrived by bulk copy: observe the stage's barrier
+      if (!(ok = mbar_wait(&bars->st_full[st], (use >> 1) & 1, abort))) break;
+      tc_fence_after();
+      // Key jk is visible from query q0 + q iff lo[q0 + q] <= jk <= q0 + q; lo is
+      // non-decreasing, so these q form one range [q_from, q_to).
+      const bool full = lo_q[BM - 1] <= k0 && k0 + BN - 1 <= q0;
+      int q_from = 0, q_to = BM;
+      if (!full) {
+        q_from = jk - q0;
+        int lo_i = 0, hi_i = BM;
+        while (lo_i < hi_i) {
+          const int m = (lo_i + hi_i) >> 1;
+          if (lo_q[m] <= jk) lo_i = m + 1; else hi_i = m;
+        }
+        q_to = lo_i;
+      }
+      q_from -= 64 * w;
+      q_to -= 64 * w;
+      float p[64];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sv[16];
+        tmem_ld16(tA + ch * 16, sv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const float4 l2 = l2_q[ch * 4 + e4];
+          const float l2v[4] = {l2.x, l2.y, l2.z, l2.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) p[ch * 16 + e4 * 4 + e] = ex2_approx(fmaf(__uint_as_float(sv[e4 * 4 + e]), c, -l2v[e]));
+        }
+        if (!full) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int q = ch * 16 + e;
+            if (q < q_from || q >= q_to) p[q] = 0.f;
+          }
+        }
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(p[ch * 16 + 2 * e], p[ch * 16 + 2 * e + 1]);
+        tmem_st8(tA + ch * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full);
+
+      // ---- dS phase
+      if (!(ok = mbar_wait(&bars->dp_full, dpf_par, abort))) break;
+      dpf_par ^= 1;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t dv[16];
+        tmem_ld16(tB + ch * 16, dv);
+        tmem_ld_wait();
+        uint32_t dk[8];
+#pragma unroll
+        for (int e4 = 0; e4 < 4; e4 += 2) {
+          const float4 d0 = dl_q[ch * 4 + e4], d1 = dl_q[ch * 4 + e4 + 1];
+          const float dlv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int q = ch * 16 + e4 * 4 + e;
+            const float s0 = p[q] * (__uint_as_float(dv[e4 * 4 + e]) - dlv[e]);
+            const float s1 = p[q + 1] * (__uint_as_float(dv[e4 * 4 + e + 1]) - dlv[e + 1]);
+            dk[(e4 * 4 + e) / 2] = pack_bf16x2(s0, s1);
+          }
+        }
+        tmem_st8(tB + ch * 16, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ds_full);
+    }
+    if (!ok) break;
+
+    // epilogue: both warpgroups write half of the columns of dV and of dK (dK scaled by 1/sqrt(D))
+    __nv_bfloat16 *dv_row = a.out0 + ((size_t(I.b) * a.S + jk) * a.H + I.h) * HD + 64 * w;
+    __nv_bfloat16 *dk_row = a.out1 + ((size_t(I.b) * a.S + jk) * a.H + I.h) * HD + 64 * w;
+    if (n > 0) {
+      if (!(ok = mbar_wait(&bars->acc_full, af_par, abort))) break;
+      af_par ^= 1;
+      tc_fence_after();
+      store_cols_bf16(tmem + lane_off + KV_COL_DV + 64 * w, 1.f, dv_row, jk < a.S);
+      store_cols_bf16(tmem + lane_off + KV_COL_DK + 64 * w, a.inv_sqrt_d, dk_row, jk < a.S);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->acc_empty);
+    } else if (jk < a.S) {
+      zero_cols_bf16(dv_row, 64);
+      zero_cols_bf16(dk_row, 64);
+    }
+  }
+  return ok;
+}
 
 __global__ void __launch_bounds__(BW_THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -527,22 +482,21 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   KvbBars *bars = reinterpret_cast<KvbBars *>(smem + KVB_SM_BAR);
-  volatile int *abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < KV_STAGES_BW; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->st_full[s], 1);
       mbar_init(&bars->st_empty[s], 1);
+      mbar_init(&bars->item_full[s], 1);
+      mbar_init(&bars->item_empty[s], 9);   // softmax 8 + MMA 1 warps
     }
     mbar_init(&bars->own_full, 1);
     mbar_init(&bars->own_empty, 1);
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(&bars->s_full[h], 1);
-      mbar_init(&bars->p_full[h], 4);
-      mbar_init(&bars->item_full[h], 1);
-      mbar_init(&bars->item_empty[h], 9);
-    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, 8);
+    mbar_init(&bars->ds_full, 8);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 1);
@@ -554,214 +508,24 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
+  if (warp == BW_PRODUCER && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    tma_prefetch_desc(&tdo);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   bool ok = true;
-
-  if (warp == BW_PRODUCER) {
-    if (lane == 0) {
-      int fill = 0, own = 0;
-      for (int it = 0;; ++it) {
-        const int slot = it & 1;
-        if (!(ok = mbar_wait(&bars->item_empty[slot], ((it >> 1) & 1) ^ 1, abort))) break;
-        const int t = atomicAdd(a.hdr + HDR_TICKET_DKDV, 1);
-        const int item = t < a.n_items ? t : -1;
-        bars->item[slot] = item;
-        mbar_arrive(&bars->item_full[slot]);
-        if (item < 0) break;
-        const BwItem I = bw_decode(a, item);
-        const TileRange R = dkdv_range(a, I);
-        if (!(ok = mbar_wait(&bars->own_empty, (it & 1) ^ 1, abort))) break;
-        mbar_arrive_expect_tx(&bars->own_full, 2 * TILE_BYTES);
-        load_tile(&tk, &bars->own_full, smem + KVB_SM_K, I.h, I.tile * BN, I.b);
-        load_tile(&tv, &bars->own_full, smem + KVB_SM_V, I.h, I.tile * BN, I.b);
-        ++own;
-        const size_t rowbase = (size_t(I.b) * a.H + I.h) * a.S_pad;
-        for (int qi = R.first; qi <= R.last && ok; ++qi) {
-          const int st = fill % KV_STAGES_BW;
-          if (!(ok = mbar_wait(&bars->st_empty[st], ((fill / KV_STAGES_BW) & 1) ^ 1, abort))) break;
-          mbar_arrive_expect_tx(&bars->st_full[st], 2 * TILE_BYTES + 3 * ROWTERM_BYTES);
-          uint8_t *dst = smem + KVB_SM_ST + st * KVB_STAGE_STRIDE;
-          load_tile(&tq, &bars->st_full[st], dst, I.h, qi * BM, I.b);
-          load_tile(&tdo, &bars->st_full[st], dst + TILE_BYTES, I.h, qi * BM, I.b);
-          bulk_load(dst + 2 * TILE_BYTES, a.lo + size_t(I.b) * a.S_pad + qi * BM, ROWTERM_BYTES, &bars->st_full[st]);
-          bulk_load(dst + 2 * TILE_BYTES + ROWTERM_BYTES, a.lse2 + rowbase + qi * BM, ROWTERM_BYTES,
-                    &bars->st_full[st]);
-          bulk_load(dst + 2 * TILE_BYTES + 2 * ROWTERM_BYTES, a.delta + rowbase + qi * BM, ROWTERM_BYTES,
-                    &bars->st_full[st]);
-          ++fill;
-        }
-        if (!ok) break;
-      }
-      bars->fill = fill;
-      bars->own_issued = own;
-    }
+  if (warp < BW_PRODUCER) {
+    ok = kv_softmax(a, smem, bars, tmem, warp >> 2, warp, lane);
+  } else if (warp == BW_PRODUCER) {
+    if (lane == 0) ok = kv_producer(&tq, &tk, &tv, &tdo, a, smem, bars);
     __syncwarp();
   } else if (warp == BW_MMA) {
-    const uint32_t k_s = smem_u32(smem + KVB_SM_K), v_s = smem_u32(smem + KVB_SM_V);
-    const uint32_t st0 = smem_u32(smem + KVB_SM_ST);
-    int use = 0, own = 0;
-    uint32_t pf_par[2] = {0, 0}, ae_par = 1;
-    for (int it = 0; ok; ++it) {
-      const int slot = it & 1;
-      if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
-      const int item = bars->item[slot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
-      if (item < 0) break;
-      const BwItem I = bw_decode(a, item);
-      const TileRange R = dkdv_range(a, I);
-      if (!(ok = mbar_wait(&bars->own_full, it & 1, abort))) break;
-      ++own;
-      tc_fence_after();
-      bool first = true;
-      if (!R.empty()) {
-        int st = use % KV_STAGES_BW;
-        if (!(ok = mbar_wait(&bars->st_full[st], (use / KV_STAGES_BW) & 1, abort))) break;
-        ++use;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t q_s = st0 + st * KVB_STAGE_STRIDE, do_s = q_s + TILE_BYTES;
-          for (int h = 0; h < 2; ++h) {
-            issue_half(tmem + col_s(h), k_s, q_s + h * HALF_ROW_BYTES);
-            issue_half(tmem + col_dp(h), v_s, do_s + h * HALF_ROW_BYTES);
-            mma_commit(&bars->s_full[h]);
-          }
-        }
-        __syncwarp();
-        for (int qi = R.first; qi <= R.last && ok; ++qi) {
-          const bool has_next = qi < R.last;
-          const uint32_t q_s = st0 + st * KVB_STAGE_STRIDE, do_s = q_s + TILE_BYTES;
-          int st2 = -1;
-          if (first) {
-            if (!(ok = mbar_wait(&bars->acc_empty, ae_par, abort))) break;
-            ae_par ^= 1;
-          }
-          for (int h = 0; h < 2 && ok; ++h) {
-            if (!(ok = mbar_wait(&bars->p_full[h], pf_par[h], abort))) break;
-            pf_par[h] ^= 1;
-            tc_fence_after();
-            if (lane == 0) {
-              issue_acc(tmem + COL_ACC0, tmem + col_s(h), do_s + h * HALF_ROW_BYTES, !first);   // dV
-              issue_acc(tmem + COL_ACC1, tmem + col_dp(h), q_s + h * HALF_ROW_BYTES, !first);   // dK
-            }
-            first = false;
-            if (h == 1 && lane == 0) mma_commit(&bars->st_empty[st]);
-            if (has_next) {
-              if (h == 0) {
-                st2 = use % KV_STAGES_BW;
-                if (!(ok = mbar_wait(&bars->st_full[st2], (use / KV_STAGES_BW) & 1, abort))) break;
-                ++use;
-                tc_fence_after();
-              }
-              if (lane == 0) {
-                const uint32_t q2 = st0 + st2 * KVB_STAGE_STRIDE, do2 = q2 + TILE_BYTES;
-                issue_half(tmem + col_s(h), k_s, q2 + h * HALF_ROW_BYTES);
-                issue_half(tmem + col_dp(h), v_s, do2 + h * HALF_ROW_BYTES);
-                mma_commit(&bars->s_full[h]);
-              }
-            }
-          }
-          __syncwarp();
-          st = st2;
-        }
-        if (!ok) break;
-      }
-      if (lane == 0) {
-        mma_commit(&bars->own_empty);
-        if (!first) mma_commit(&bars->acc_full);
-      }
-      __syncwarp();
-    }
-    if (lane == 0) {
-      bars->use = use;
-      bars->own_used = own;
-    }
-  } else if (warp < 8) {
-    const int h = warp >> 2;   // query half this warpgroup owns
-    const int r = (warp & 3) * 32 + lane;
-    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_off + col_s(h), tP = tmem + lane_off + col_dp(h);
-    const float c = a.scale_log2;
-    uint32_t sf_par = 0, af_par = 0;
-    int use = 0;
-    for (int it = 0; ok; ++it) {
-      const int slot = it & 1;
-      if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
-      const int item = bars->item[slot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
-      if (item < 0) break;
-      const BwItem I = bw_decode(a, item);
-      const TileRange R = dkdv_range(a, I);
-      const int k0 = I.tile * BN, j = k0 + r;
-      const int *lr = a.lo + size_t(I.b) * a.S_pad;
-      for (int qi = R.first; qi <= R.last; ++qi) {
-        const int st = use % KV_STAGES_BW;
-        const uint32_t st_par = (use / KV_STAGES_BW) & 1;
-        ++use;
-        if (!(ok = mbar_wait(&bars->s_full[h], sf_par, abort))) break;
-        sf_par ^= 1;
-        // the stage's lo / lse2 / delta rows arrived by bulk copy: observe their barrier
-        if (!(ok = mbar_wait(&bars->st_full[st], st_par, abort))) break;
-        tc_fence_after();
-        const uint8_t *stage = smem + KVB_SM_ST + st * KVB_STAGE_STRIDE;
-        const int *lo_q = reinterpret_cast<const int *>(stage + 2 * TILE_BYTES) + h * HALF_ROWS;
-        const float *l2_q = reinterpret_cast<const float *>(stage + 2 * TILE_BYTES + ROWTERM_BYTES) + h * HALF_ROWS;
-        const float *dl_q = reinterpret_cast<const float *>(stage + 2 * TILE_BYTES + 2 * ROWTERM_BYTES) + h * HALF_ROWS;
-        const int q0 = qi * BM;
-        const bool full = pair_full(lr, q0, k0);
-        const int qb = q0 + h * HALF_ROWS;   // first query of this half
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(tS + ch * 32, sv);
-          tmem_ld32(tP + ch * 32, dv);
-          tmem_ld_wait();
-          uint32_t pk[16], dk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float pp[2], dd[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int cidx = ch * 32 + 2 * e + u;
-              float p = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), c, -l2_q[cidx]));
-              if (!full) {
-                const int qq = qb + cidx;
-                if (j < lo_q[cidx] || j > qq) p = 0.f;
-              }
-              pp[u] = p;
-              dd[u] = p * (__uint_as_float(dv[2 * e + u]) - dl_q[cidx]);
-            }
-            pk[e] = pack_bf16x2(pp[0], pp[1]);
-            dk[e] = pack_bf16x2(dd[0], dd[1]);
-          }
-          tmem_st16(tS + ch * 16, pk);
-          tmem_st16(tP + ch * 16, dk);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_full[h]);
-      }
-      if (!ok) break;
-      // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (scaled by 1/sqrt(D))
-      __nv_bfloat16 *dst = (h == 0 ? a.out0 : a.out1) + ((size_t(I.b) * a.S + j) * a.H + I.h) * HD;
-      if (!R.empty()) {
-        if (!(ok = mbar_wait(&bars->acc_full, af_par, abort))) break;
-        af_par ^= 1;
-        tc_fence_after();
-        store_row_bf16(tmem + lane_off + (h == 0 ? COL_ACC0 : COL_ACC1), HD, h == 0 ? 1.f : a.inv_sqrt_d, dst,
-                       j < a.S);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->acc_empty);
-      } else if (j < a.S) {
-        zero_row_bf16(dst, HD);
-      }
-    }
+    ok = kv_mma(a, smem, bars, tmem, lane);
   }
 
   if (!ok) {
@@ -772,8 +536,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   __syncthreads();
   if (bars->abort) {
     if (warp == BW_PRODUCER && lane == 0) {
-      for (int n = bars->use; n < bars->fill; ++n)
-        bounded_wait_plain_bw(&bars->st_full[n % KV_STAGES_BW], (n / KV_STAGES_BW) & 1);
+      for (int k = bars->use; k < bars->fill; ++k) bounded_wait_plain_bw(&bars->st_full[k & 1], (k >> 1) & 1);
       if (bars->own_issued > bars->own_used) bounded_wait_plain_bw(&bars->own_full, (bars->own_issued - 1) & 1);
     }
     if (warp == BW_MMA && lane == 0) {
@@ -796,6 +559,342 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   }
 }
 
+// ============================================================================= dQ
+// Item: (b, h, query tile). Resident: Q and dO; the rows' lo / lse2 / delta live in
+// registers (thread = query row). Streamed: K_j (ring of three) and V_j (ring of two).
+// Per key tile j:
+//   S    = Q . K_j^T  -> A_{j % 2}      dP = dO . V_j^T -> B
+//   P    = exp2(S c - lse2) (masked),  dS = P (dP - delta)  -> bf16 over A_{j % 2}
+//   dQ  += dS . K_j   (C; scaled by 1/sqrt(D) in the epilogue)
+// TMEM: A0 [0, 128), A1 [128, 256), B [256, 384), C [384, 512). Tensor-core order:
+// dQ(j), dP(j+1), S(j+2): the P phase of tile j+1 runs under dQ(j) and dP(j+1), its dS
+// phase under S(j+2). Deterministic: every dQ row is summed by one CTA in a fixed order.
+constexpr int DQ_KSTAGES = 3, DQ_VSTAGES = 2;
+constexpr int DQ_SM_Q = 0, DQ_SM_DO = TILE_BYTES, DQ_SM_K = 2 * TILE_BYTES;
+constexpr int DQ_SM_V = DQ_SM_K + DQ_KSTAGES * TILE_BYTES;
+constexpr int DQ_SM_BAR = DQ_SM_V + DQ_VSTAGES * TILE_BYTES;
+constexpr uint32_t DQ_COL_B = 256, DQ_COL_C = 384;
+
+struct DqBars {
+  uint64_t k_full[DQ_KSTAGES], k_empty[DQ_KSTAGES], v_full[DQ_VSTAGES], v_empty[DQ_VSTAGES];
+  uint64_t own_full, own_empty;
+  uint64_t s_full[2], dp_full, ds_full;
+  uint64_t acc_full, acc_empty;
+  uint64_t item_full[2], item_empty[2];
+  uint64_t drain;
+  int item[2];
+  uint32_t tmem_base;
+  int abort;
+  int k_fill, k_use, v_fill, v_use, own_issued, own_used;
+};
+constexpr int DQ_SMEM = DQ_SM_BAR + int(sizeof(DqBars)) + 1024;
+static_assert(DQ_SMEM <= 232448, "shared memory budget of one CTA");
+
+__device__ __forceinline__ bool dq_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
+                                            const CUtensorMap *tdo, const BwArgs &a, uint8_t *smem, DqBars *bars) {
+  volatile int *abort = &bars->abort;
+  int k_fill = 0, v_fill = 0, own = 0;
+  bool ok = true;
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_empty[slot], ((it >> 1) & 1) ^ 1, abort))) break;
+    const int t = atomicAdd(a.hdr + HDR_TICKET_DQ, 1);
+    const int item = t < a.n_items ? t : -1;
+    bars->item[slot] = item;
+    mbar_arrive(&bars->item_full[slot]);
+    if (item < 0) break;
+    const BwItem I = bw_decode(a, item);
+    const TileRange R = dq_range(a, I);
+    const int n = range_tiles(R);
+    if (!(ok = mbar_wait(&bars->own_empty, (it & 1) ^ 1, abort))) break;
+    mbar_arrive_expect_tx(&bars->own_full, 2 * TILE_BYTES);
+    load_tile(tq, &bars->own_full, smem + DQ_SM_Q, I.h, I.tile * BM, I.b);
+    load_tile(tdo, &bars->own_full, smem + DQ_SM_DO, I.h, I.tile * BM, I.b);
+    ++own;
+    // K_j, then V_j: each ring is refilled as soon as its oldest tile is released
+    for (int j = 0; j < n && ok; ++j) {
+      const int row0 = (R.first + j) * BN;
+      const int ks = k_fill % DQ_KSTAGES;
+      if (!(ok = mbar_wait(&bars->k_empty[ks], ((k_fill / DQ_KSTAGES) & 1) ^ 1, abort))) break;
+      mbar_arrive_expect_tx(&bars->k_full[ks], TILE_BYTES);
+      load_tile(tk, &bars->k_full[ks], smem + DQ_SM_K + ks * TILE_BYTES, I.h, row0, I.b);
+      ++k_fill;
+      const int vs = v_fill % DQ_VSTAGES;
+      if (!(ok = mbar_wait(&bars->v_empty[vs], ((v_fill / DQ_VSTAGES) & 1) ^ 1, abort))) break;
+      mbar_arrive_expect_tx(&bars->v_full[vs], TILE_BYTES);
+      load_tile(tv, &bars->v_full[vs], smem + DQ_SM_V + vs * TILE_BYTES, I.h, row0, I.b);
+      ++v_fill;
+    }
+    if (!ok) break;
+  }
+  bars->k_fill = k_fill;
+  bars->v_fill = v_fill;
+  bars->own_issued = own;
+  return ok;
+}
+
+__device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *bars, uint32_t tmem, int lane) {
+  volatile int *abort = &bars->abort;
+  const uint32_t q_s = smem_u32(smem + DQ_SM_Q), do_s = smem_u32(smem + DQ_SM_DO);
+  const uint32_t k0_s = smem_u32(smem + DQ_SM_K), v0_s = smem_u32(smem + DQ_SM_V);
+  int k_use = 0, v_use = 0, own = 0;
+  uint32_t dsf_par = 0, ae_par = 1;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
+    const int item = bars->item[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+    if (item < 0) break;
+    const BwItem I = bw_decode(a, item);
+    const int n = range_tiles(dq_range(a, I));
+    if (!(ok = mbar_wait(&bars->own_full, it & 1, abort))) break;
+    ++own;
+    tc_fence_after();
+    const int kb = k_use, vb = v_use;
+    auto k_s = [&](int j) { return k0_s + uint32_t((kb + j) % DQ_KSTAGES) * TILE_BYTES; };
+    auto v_s = [&](int j) { return v0_s + uint32_t((vb + j) % DQ_VSTAGES) * TILE_BYTES; };
+    auto issue_s = [&](int j) -> bool {   // S(j) = Q K_j^T into A_{j % 2}
+      if (!mbar_wait(&bars->k_full[(kb + j) % DQ_KSTAGES], ((kb + j) / DQ_KSTAGES) & 1, abort)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        mma_tile_kk(tmem + uint32_t(j & 1) * 128, q_s, k_s(j), false);
+        mma_commit(&bars->s_full[j & 1]);
+      }
+      __syncwarp();
+      return true;
+    };
+    auto issue_dp = [&](int j) -> bool {   // dP(j) = dO V_j^T into B; V_j is then released
+      if (!mbar_wait(&bars->v_full[(vb + j) % DQ_VSTAGES], ((vb + j) / DQ_VSTAGES) & 1, abort)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        mma_tile_kk(tmem + DQ_COL_B, do_s, v_s(j), false);
+        mma_commit(&bars->dp_full);
+        mma_commit(&bars->v_empty[(vb + j) % DQ_VSTAGES]);
+      }
+      __syncwarp();
+      return true;
+    };
+    if (n > 0) ok = issue_s(0) && issue_dp(0) && (n < 2 || issue_s(1));
+    for (int j = 0; j < n && ok; ++j) {
+      if (!(ok = mbar_wait(&bars->ds_full, dsf_par, abort))) break;
+      dsf_par ^= 1;
+      if (j == 0) {
+        if (!(ok = mbar_wait(&bars->acc_empty, ae_par, abort))) break;
+        ae_par ^= 1;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        mma_tile_ts(tmem + DQ_COL_C, tmem + uint32_t(j & 1) * 128, k_s(j), j > 0);   // dQ += dS K
+        mma_commit(&bars->k_empty[(kb + j) % DQ_KSTAGES]);
+      }
+      __syncwarp();
+      if (j + 1 < n && !(ok = issue_dp(j + 1))) break;
+      if (j + 2 < n && !(ok = issue_s(j + 2))) break;
+    }
+    if (!ok) break;
+    k_use = kb + n;
+    v_use = vb + n;
+    if (lane == 0) {
+      if (n > 0) mma_commit(&bars->acc_full);
+      mma_commit(&bars->own_empty);
+    }
+    __syncwarp();
+  }
+  if (lane == 0) {
+    bars->k_use = k_use;
+    bars->v_use = v_use;
+    bars->own_used = own;
+  }
+  return ok;
+}
+
+// Softmax warpgroup w of the dQ kernel: thread = query row `row`; key columns
+// [64 w, 64 w + 64) of every streamed tile.
+__device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32_t tmem, int w, int warp, int lane) {
+  volatile int *abort = &bars->abort;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+  const uint32_t tB = tmem + lane_off + DQ_COL_B + 64 * w;
+  const float c = a.scale_log2;
+  uint32_t sf_par[2] = {0, 0}, dpf_par = 0, af_par = 0;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
+    const int item = bars->item[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+    if (item < 0) break;
+    const BwItem I = bw_decode(a, item);
+    const TileRange R = dq_range(a, I);
+    const int n = range_tiles(R);
+    const int q0 = I.tile * BM, i = q0 + row;   // this thread's query
+    const int *lr = a.lo + size_t(I.b) * a.S_pad;
+    const size_t rowterm = (size_t(I.b) * a.H + I.h) * a.S_pad + i;
+    const int lo_i = lr[i];
+    const int lo_last = lr[q0 + BM - 1];
+    const float l2 = a.lse2[rowterm], dl = a.delta[rowterm];
+    for (int j = 0; j < n; ++j) {
+      const int k0 = (R.first + j) * BN;
+      const uint32_t tA = tmem + lane_off + uint32_t(j & 1) * 128 + 64 * w;
+      const bool full = lo_last <= k0 && k0 + BN - 1 <= q0;
+      // visible keys of query i: lo_i <= key <= i, i.e. columns [c_from, c_to) here
+      const int c_from = lo_i - k0 - 64 * w, c_to = i - k0 - 64 * w + 1;
+
+      // ---- P phase
+      if (!(ok = mbar_wait(&bars->s_full[j & 1], sf_par[j & 1], abort))) break;
+      sf_par[j & 1] ^= 1;
+      tc_fence_after();
+      float p[64];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sv[16];
+        tmem_ld16(tA + ch * 16, sv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) p[ch * 16 + e] = ex2_approx(fmaf(__uint_as_float(sv[e]), c, -l2));
+        if (!full) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int cc = ch * 16 + e;
+            if (cc < c_from || cc >= c_to) p[cc] = 0.f;
+          }
+        }
+      }
+
+      // ---- dS phase
+      if (!(ok = mbar_wait(&bars->dp_full, dpf_par, abort))) break;
+      dpf_par ^= 1;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t dv[16];
+        tmem_ld16(tB + ch * 16, dv);
+        tmem_ld_wait();
+        uint32_t dk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          dk[e] = pack_bf16x2(p[ch * 16 + 2 * e] * (__uint_as_float(dv[2 * e]) - dl),
+                              p[ch * 16 + 2 * e + 1] * (__uint_as_float(dv[2 * e + 1]) - dl));
+        tmem_st8(tA + ch * 16, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ds_full);
+    }
+    if (!ok) break;
+
+    __nv_bfloat16 *dst = a.out0 + ((size_t(I.b) * a.S + i) * a.H + I.h) * HD + 64 * w;
+    if (n > 0) {
+      if (!(ok = mbar_wait(&bars->acc_full, af_par, abort))) break;
+      af_par ^= 1;
+      tc_fence_after();
+      store_cols_bf16(tmem + lane_off + DQ_COL_C + 64 * w, a.inv_sqrt_d, dst, i < a.S);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->acc_empty);
+    } else if (i < a.S) {
+      zero_cols_bf16(dst, 64);
+    }
+  }
+  return ok;
+}
+
+__global__ void __launch_bounds__(BW_THREADS, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const BwArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DqBars *bars = reinterpret_cast<DqBars *>(smem + DQ_SM_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < DQ_KSTAGES; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < DQ_VSTAGES; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->item_full[s], 1);
+      mbar_init(&bars->item_empty[s], 9);   // softmax 8 + MMA 1 warps
+    }
+    mbar_init(&bars->own_full, 1);
+    mbar_init(&bars->own_empty, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->ds_full, 8);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, 8);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    bars->k_fill = bars->k_use = bars->v_fill = bars->v_use = bars->own_issued = bars->own_used = 0;
+    fence_mbar_init();
+  }
+  if (warp == BW_MMA) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == BW_PRODUCER && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    tma_prefetch_desc(&tdo);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  bool ok = true;
+  if (warp < BW_PRODUCER) {
+    ok = dq_softmax(a, bars, tmem, warp >> 2, warp, lane);
+  } else if (warp == BW_PRODUCER) {
+    if (lane == 0) ok = dq_producer(&tq, &tk, &tv, &tdo, a, smem, bars);
+    __syncwarp();
+  } else if (warp == BW_MMA) {
+    ok = dq_mma(a, smem, bars, tmem, lane);
+  }
+
+  if (!ok) {
+    bars->abort = 1;
+    raise_error(a.hdr + HDR_ERR, ERRBIT_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (bars->abort) {
+    if (warp == BW_PRODUCER && lane == 0) {
+      for (int k = bars->k_use; k < bars->k_fill; ++k)
+        bounded_wait_plain_bw(&bars->k_full[k % DQ_KSTAGES], (k / DQ_KSTAGES) & 1);
+      for (int k = bars->v_use; k < bars->v_fill; ++k)
+        bounded_wait_plain_bw(&bars->v_full[k % DQ_VSTAGES], (k / DQ_VSTAGES) & 1);
+      if (bars->own_issued > bars->own_used) bounded_wait_plain_bw(&bars->own_full, (bars->own_issued - 1) & 1);
+    }
+    if (warp == BW_MMA && lane == 0) {
+      mma_commit(&bars->drain);
+      bounded_wait_plain_bw(&bars->drain, 0);
+    }
+    __syncthreads();
+  }
+  if (warp == BW_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.hdr + HDR_DONE_DQ, 1) == int(gridDim.x) - 1) {
+      a.hdr[HDR_TICKET_DQ] = 0;
+      a.hdr[HDR_DONE_DQ] = 0;
+      __threadfence();
+    }
+  }
+}
+
 BwArgs bw_args(const Problem &p, void *workspace, const int *list) {
   const Workspace w = Workspace::layout(p.B, p.S, p.H);
   char *base = static_cast<char *>(workspace);
@@ -812,7 +911,8 @@ BwArgs bw_args(const Problem &p, void *workspace, const int *list) {
   a.H = p.H;
   a.nT = w.nT;
   a.S_pad = w.S_pad;
-  a.n_items = p.B * w.nT * p.H;
+  a.n_list = p.B * w.nT;
+  a.n_items = a.n_list * p.H;
   a.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
   a.inv_sqrt_d = 1.f / sqrtf(float(HD));
   return a;

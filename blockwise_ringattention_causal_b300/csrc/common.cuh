@@ -284,6 +284,35 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v) {
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ----------------------------------------------------------------------------- 128x128x128 products
+// Instruction descriptors of the 128 x 128 (M x N) bf16 products with fp32 accumulation.
+constexpr uint32_t IDESC_128_KK = idesc_bf16(128, 128, false, false);   // A, B both K-major
+constexpr uint32_t IDESC_128_KM = idesc_bf16(128, 128, false, true);    // A K-major (or TMEM), B MN-major
+constexpr uint32_t IDESC_128_MM = idesc_bf16(128, 128, true, true);     // A, B both MN-major
+
+// D[128 x 128] (+)= A[128 rows x 128] . B[128 rows x 128]^T over the 128-wide inner
+// dimension; both operands are 128-row tiles stored as two 64-column 128B-swizzled
+// boxes HALF_BYTES apart (K-major: rows 128 bytes apart, 8-row groups 1024 bytes apart).
+__device__ __forceinline__ void mma_tile_kk(uint32_t d_tmem, uint32_t a_s, uint32_t b_s, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t off = uint32_t(kk >> 2) * HALF_BYTES + uint32_t(kk & 3) * 32;
+    mma_ss(d_tmem, sdesc_sw128(a_s + off, 16, 1024), sdesc_sw128(b_s + off, 16, 1024), IDESC_128_KK,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// D[128 x 128] (+)= X[128 x 128] . Y[128 x 128] with X bf16 in TMEM (the inner block kk
+// of 16 at column x_tmem + 16 kk, 8 packed columns) and Y a 128-row tile read MN-major
+// (its rows are the inner dimension: 16 rows = two 8-row groups of 1024 bytes; the two
+// 64-column boxes HALF_BYTES apart are the N halves).
+__device__ __forceinline__ void mma_tile_ts(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_s, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts(d_tmem, x_tmem + uint32_t(kk) * 16, sdesc_sw128(y_s + uint32_t(kk) * 2048, HALF_BYTES, 1024),
+           IDESC_128_KM, (accumulate || kk > 0) ? 1u : 0u);
+}
+
 // ----------------------------------------------------------------------------- tile ranges
 // Inclusive range of key tiles that query tile [q0, q0+BM) of one batch row needs.
 // `lo_row[i]` is the first key visible to query i (its document start; i+1 for

@@ -79,8 +79,9 @@ typedef enum {
 size_t lwm_attn_workspace_size(int B, int S, int H, int D);
 
 /* The leading part of that workspace which every call except the single-kernel
- * backward pass uses (no dQ accumulator): enough for lwm_attn_prepare, the forward
- * entry points and the LWM_BWD_DELTA / LWM_BWD_DKDV / LWM_BWD_DQ stages. */
+ * backward stage LWM_BWD_FUSED uses (no dQ accumulator): enough for lwm_attn_prepare,
+ * the forward entry points, lwm_attn_bwd, lwm_attn_bwd_prepared and the LWM_BWD_DELTA /
+ * LWM_BWD_DKDV / LWM_BWD_DQ stages. */
 size_t lwm_attn_workspace_size_fwd(int B, int S, int H, int D);
 
 /* Metadata pre-pass alone: validates seg_ids/pos and writes segment starts, per-tile
@@ -114,12 +115,9 @@ lwm_status lwm_attn_fwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm
                                  void *workspace, size_t workspace_bytes, lwm_stream stream);
 
 /* Backward pass: metadata pre-pass, the row-dot pre-pass delta_i = dout_i . out_i,
- * then the single-kernel backward pass (LWM_BWD_FUSED below). `out` and `lse` are the
+ * then the dK/dV kernel and the dQ kernel (LWM_BWD_ALL below). `out` and `lse` are the
  * forward outputs. dq, dk, dv are fully overwritten (no accumulation into existing
- * values). dk and dv are bitwise reproducible; dq is summed in fp32 in an order that
- * depends on scheduling (run-to-run differences at the level of fp32 rounding before
- * the bf16 conversion). LWM_BWD_ALL through lwm_attn_bwd_stages gives a bitwise
- * reproducible dq. The workspace must have lwm_attn_workspace_size() bytes. */
+ * values) and bitwise reproducible. */
 lwm_status lwm_attn_bwd(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
                         const lwm_bf16 *out, const lwm_bf16 *dout, const float *lse,
                         const int32_t *seg_ids, const int32_t *pos,
@@ -128,7 +126,7 @@ lwm_status lwm_attn_bwd(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
                         lwm_stream stream);
 
 /* Backward pass reusing the metadata of a previous lwm_attn_prepare in `workspace`
- * (same stages as lwm_attn_bwd: LWM_BWD_DELTA | LWM_BWD_FUSED). */
+ * (same stages as lwm_attn_bwd: LWM_BWD_ALL). */
 lwm_status lwm_attn_bwd_prepared(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
                                  const lwm_bf16 *out, const lwm_bf16 *dout, const float *lse,
                                  lwm_bf16 *dq, lwm_bf16 *dk, lwm_bf16 *dv,
@@ -144,8 +142,12 @@ typedef enum {
   LWM_BWD_FUSED = 8   /* dk, dv and dq in one kernel from one recomputation of the
                          probabilities (5 tensor-core products per tile pair instead of
                          7): dq is accumulated in fp32 in the workspace's dQ accumulator
-                         (zeroed by the stage itself) and then converted to bf16. Needs
-                         LWM_BWD_DELTA's results; cannot be combined with DKDV or DQ */
+                         (zeroed by the stage itself) and then converted to bf16, in an
+                         order that depends on scheduling (dq is not bitwise reproducible;
+                         dk, dv are). Needs LWM_BWD_DELTA's results and the whole
+                         lwm_attn_workspace_size() workspace; cannot be combined with DKDV
+                         or DQ. On B300 it is slower than DKDV + DQ: moving dQ out through
+                         shared memory competes with the tensor core for bandwidth */
 } lwm_bwd_stage;
 
 /* Runs the selected backward stages in the order delta, fused, dK/dV, dQ, reusing the
