@@ -142,12 +142,15 @@ def oracle_sample(S_sample, heads, seed=0):
     tokens of `heads` heads of a single causal document. Returns (seconds, credited
     flops, threads)."""
     import oracle
+    cpus = len(os.sched_getaffinity(0))
     try:
         from threadpoolctl import threadpool_info
         threads = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
     except ImportError:
-        threads = 1
-    threads = min(threads, len(os.sched_getaffinity(0)))
+        # numpy's bundled OpenBLAS starts one thread per available CPU unless told otherwise
+        env = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+        threads = int(env) if env and env.isdigit() else cpus
+    threads = min(threads, cpus)
     g = torch.Generator().manual_seed(seed)
     q, k, v, do = (torch.randn((1, S_sample, heads, 128), generator=g).to(torch.bfloat16).float().numpy()
                    for _ in range(4))
@@ -209,7 +212,7 @@ def run_ours(args, rank, world):
     lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
     if w.backward:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = lwm.new_workspace(B, S, H, D, dev)
+    ws = lwm.new_workspace(B, S, H, D, dev, forward_only=not w.backward)
     stream = torch.cuda.current_stream()
     pairs = I.pairs_per_head(w)
     flops_fwd = 4.0 * D * H * pairs
@@ -343,7 +346,7 @@ def run_ours(args, rank, world):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        S_sample, heads = 8192, 6
+        S_sample, heads = 8192, 8
         dt, fl, threads = oracle_sample(S_sample, heads)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"float64 oracle forward+backward of {heads} heads x first {S_sample} tokens of one "

@@ -134,3 +134,42 @@ def test_causal_s32k_sampled(cuda_device, deterministic):
 
 def test_packed_mixed_s64k_sampled(cuda_device):
     _sampled_bwd(3, cuda_device, key_heads=(5,))
+
+
+def test_video_s256k_sampled_and_invariants(cuda_device):
+    """256K tokens (1024 frames of 256 tokens with a shared per-frame offset).
+
+    dq on 512 sampled query rows of a subset of heads (exact from each row alone); dk, dv
+    on the last 256 keys of two heads (exact from the rows that see them); and on every
+    head the identities that hold at any size: sum_j dv_j = sum_i dout_i (each row's
+    probabilities sum to 1) and sum_j dk_j = 0 (each row's dS sums to 0).
+    """
+    w = I.workload(4)
+    x = I.make_inputs(w, cuda_device)
+    _, _, dq, dk, dv = run_fwd_bwd(x)
+    seg = x["seg"].cpu().numpy()
+    rows = I.sample_rows(w.S)
+    got, ref = [], []
+    for h in (0, 13, 31):
+        q, k, v, do = (x[n][0:1, :, h:h + 1].float().cpu().numpy() for n in ("q", "k", "v", "dout"))
+        for c in range(0, len(rows), 64):
+            r = rows[c:c + 64]
+            ref.append(oracle.attention_backward_rows(q, k, v, do, seg[0:1], 0, r)[:, 0])
+            got.append(f64(dq[0, r, h]))
+    e_dq = rel_l2(np.concatenate(got), np.concatenate(ref))
+    keys = np.arange(w.S - 256, w.S)
+    gk, gv, rk, rv = [], [], [], []
+    for h in (4, 22):
+        q, k, v, do = (x[n][0:1, :, h:h + 1].float().cpu().numpy() for n in ("q", "k", "v", "dout"))
+        kk, vv = oracle.attention_key_grads(q, k, v, do, seg[0:1], 0, 0, keys)
+        gk.append(f64(dk[0, keys, h])); rk.append(kk)
+        gv.append(f64(dv[0, keys, h])); rv.append(vv)
+    e_dk = rel_l2(np.concatenate(gk), np.concatenate(rk))
+    e_dv = rel_l2(np.concatenate(gv), np.concatenate(rv))
+    assert max(e_dq, e_dk, e_dv) <= GRAD_REL, f"dq {e_dq:.2e} dk {e_dk:.2e} dv {e_dv:.2e}"
+    # identities over all heads, in float64 on the device
+    sum_dv = dv[0].double().sum(dim=0)            # [H, D]
+    sum_do = x["dout"][0].double().sum(dim=0)
+    assert float((sum_dv - sum_do).norm() / sum_do.norm()) <= GRAD_REL
+    sum_dk = dk[0].double().sum(dim=0)
+    assert float(sum_dk.norm() / dk[0].double().norm()) <= GRAD_REL

@@ -18,7 +18,9 @@ pytestmark = pytest.mark.gpu
 
 
 def run_fwd(x, kv_chunks=1):
-    out, lse, ws = lwm.forward(x["q"], x["k"], x["v"], x.get("seg"), x.get("pos"), kv_chunks=kv_chunks)
+    B, S, H, D = x["q"].shape
+    ws = lwm.new_workspace(B, S, H, D, x["q"].device, forward_only=True)
+    out, lse, ws = lwm.forward(x["q"], x["k"], x["v"], x.get("seg"), x.get("pos"), kv_chunks=kv_chunks, workspace=ws)
     assert lwm.lwm_attn_check(ws) == 0
     return out, lse
 
@@ -133,3 +135,42 @@ def test_causal_s32k_sampled_rows(cuda_device):
 
 def test_packed_mixed_s64k_sampled_rows(cuda_device):
     _sampled(3, cuda_device)
+
+
+# ----------------------------------------------------------------------------- 256K and 1M tokens
+# The whole-row oracle is exact but costs O(rows x S x D) host flops per head, so at
+# S >= 256K it runs on 512 sampled query rows of a spread subset of heads.
+SAMPLED_HEADS_256K = (0, 9, 18, 27)
+SAMPLED_HEADS_1M = (0, 21)
+
+
+def _sampled_heads(w, x, out, lse, heads, rows_per_call):
+    rows = I.sample_rows(w.S)
+    seg = x["seg"].cpu().numpy()
+    got_o, got_l, ref_o, ref_l = [], [], [], []
+    for h in heads:
+        q, k, v = (x[n][0:1, :, h:h + 1].float().cpu().numpy() for n in ("q", "k", "v"))
+        for c in range(0, len(rows), rows_per_call):
+            r = rows[c:c + rows_per_call]
+            o, l = oracle.attention_forward_rows(q, k, v, seg[0:1], 0, r)
+            ref_o.append(o[:, 0]); ref_l.append(l[0])
+            got_o.append(f64(out[0, r, h])); got_l.append(f64(lse[0, h, r]))
+    assert_fwd(np.concatenate(got_o), np.concatenate(got_l), np.concatenate(ref_o), np.concatenate(ref_l),
+               f"{w.name} heads {heads}")
+
+
+def test_video_s256k_sampled_rows(cuda_device):
+    w = I.workload(4)
+    x = I.make_inputs(w, cuda_device, with_dout=False)
+    out, lse = run_fwd(x, kv_chunks=w.kv_chunks)
+    _sampled_heads(w, x, out, lse, SAMPLED_HEADS_256K, 64)
+
+
+def test_ring_order_s1m_sampled_rows(cuda_device):
+    """1M tokens in one launch, key/value chunks visited in ring order (8 chunks)."""
+    w = I.workload(5)
+    assert w.kv_chunks == 8 and not w.backward
+    x = I.make_inputs(w, cuda_device, with_dout=False)
+    out, lse = run_fwd(x, kv_chunks=w.kv_chunks)
+    assert torch.isfinite(lse).all()
+    _sampled_heads(w, x, out, lse, SAMPLED_HEADS_1M, 16)
