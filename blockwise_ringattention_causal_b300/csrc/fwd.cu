@@ -10,7 +10,7 @@
 // key/value tiles below; kv_chunks > 1 visits the tiles in ring order.
 //
 // One persistent CTA per SM takes work items (b, h, pair of 128-row query tiles) from
-// a longest-first list through an atomic ticket. Warp roles:
+// a head-major, longest-first list through an atomic ticket. Warp roles:
 //   warps 0-3  softmax for query tile 0 (one TMEM lane = one query row per thread)
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer (and the scheduler ticket)
@@ -62,7 +62,7 @@ struct FwdArgs {
   int *hdr;
   __nv_bfloat16 *out;
   float *lse;
-  int B, S, H, nP, n_items, S_pad;
+  int B, S, H, nP, n_list, n_items, S_pad;
   float scale_log2;   // log2(e) / sqrt(D)
 };
 
@@ -70,9 +70,12 @@ struct Item {
   int b, h, pair;
 };
 
+// Items of one head are consecutive (head-major), each head's query-tile pairs longest
+// first, so that the CTAs running at the same time stream the same head's K and V
+// through L2.
 __device__ __forceinline__ Item decode(const FwdArgs &a, int item) {
-  const int e = a.list[item / a.H];
-  return {e / a.nP, item % a.H, e % a.nP};
+  const int e = a.list[item % a.n_list];
+  return {e / a.nP, item / a.n_list, e % a.nP};
 }
 
 // S = Q K^T over D = 128: 8 MMAs of K = 16; each 64-dim half of a tile is one
@@ -517,7 +520,8 @@ cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   a.H = p.H;
   a.nP = w.nP;
   a.S_pad = w.S_pad;
-  a.n_items = p.B * w.nP * p.H;
+  a.n_list = p.B * w.nP;
+  a.n_items = a.n_list * p.H;
   a.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
   const int grid = a.n_items < p.num_sms ? a.n_items : p.num_sms;
   fwd_kernel<<<grid, FWD_THREADS, FWD_SMEM, stream>>>(tq, tk, tv, a);
