@@ -44,12 +44,21 @@ def load_peaks():
         return {"bf16": 1800.0, "bf16_sustained": 1400.0, "hbm": 6400.0, "source": "fallback"}
 
 
-def load_traffic():
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu record, or
+    None when there is none or the kernel's source has changed since it was taken."""
+    import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
-            return json.load(f)
-    except (OSError, ValueError):
-        return {}
+            rec = json.load(f).get(kernel)
+        if not rec:
+            return None
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha1(f.read()).hexdigest() != rec["sha1"]:
+                return None
+        return rec["bytes_per_launch"].get(workload)
+    except (OSError, ValueError, KeyError):
+        return None
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -290,7 +299,7 @@ def run_ours(args, rank, world):
     dom = max((n for n in alg if n in per_kernel), key=lambda n: per_kernel[n])
     peaks = load_peaks()
     achieved = alg[dom] / (per_kernel[dom] * 1e-3) / 1e12
-    traffic = load_traffic().get(f"{dom}_kernel", {}).get(w.name)
+    traffic = load_traffic(f"{dom}_kernel", w.name)
     roofline = {"bound": "tensor", "kernel": f"{dom}_kernel", "achieved": achieved, "peak": peaks["bf16"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} bf16 burst", "peak_sustained": peaks["bf16_sustained"],
