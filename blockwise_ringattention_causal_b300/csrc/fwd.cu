@@ -232,6 +232,9 @@ __device__ bool mma_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_
             if (lane == 0) issue_pv(tmem + col_o(t), tmem + col_s(t), kv_s0 + stV * TILE_BYTES, !first[t]);
             first[t] = false;
           }
+          // V(cur) is free once both P.V products are done: release it before S1(next)
+          // is queued, so that the producer can refill its stage half a step earlier.
+          if (t == 1 && lane == 0) mma_commit(&bars->kv_empty[stV]);
           if (has_next) {
             if (t == 0 && !(ok = wait_kv(stK2))) break;
             if (lane == 0 && R.r[t].has(nxt)) {
@@ -241,10 +244,7 @@ __device__ bool mma_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_
           }
         }
         if (!ok) break;
-        if (lane == 0) {
-          if (has_next) mma_commit(&bars->kv_empty[stK2]);
-          mma_commit(&bars->kv_empty[stV]);
-        }
+        if (lane == 0 && has_next) mma_commit(&bars->kv_empty[stK2]);
         __syncwarp();
         if (!has_next) break;
       }
@@ -318,9 +318,15 @@ __device__ bool softmax_role(const FwdArgs &a, FwdBars *bars, uint32_t tmem, int
           if (j < lo_i || j > i) s[cc] = 0xff800000u;   // -inf
         }
       }
-      float mx = NEG_INF;
+      // row max: four independent chains of 3-input max
+      float mq[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
 #pragma unroll
-      for (int cc = 0; cc < BN; ++cc) mx = fmaxf(mx, __uint_as_float(s[cc]));
+      for (int cc = 0; cc < BN; cc += 8) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          mq[u] = max3f(mq[u], __uint_as_float(s[cc + 2 * u]), __uint_as_float(s[cc + 2 * u + 1]));
+      }
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       const float m_new = fmaxf(m, mx * c);
       // Rescale only when the running max grew by more than 8 (log2 units); otherwise
       // keep the stale max: p <= 2^8 stays exact in fp32 and the final o = O / l uses
@@ -333,6 +339,30 @@ __device__ bool softmax_role(const FwdArgs &a, FwdBars *bars, uint32_t tmem, int
       }
       const bool fix_o = resc && had && l > 0.f;
       l *= alpha;
+      const float m_use = (m == NEG_INF) ? 0.f : m;
+      // p = exp2(s c - m) two at a time (paired fma and add), P written back as bf16
+      const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_use, -m_use);
+      uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+      for (int cc = 0; cc < BN; cc += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[cc + 2 * e]), __uint_as_float(s[cc + 2 * e + 1])), c2, nm2), x0,
+                    x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          acc[e & 1] = f2_add(acc[e & 1], f2_pack(p0, p1));
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + cc / 2, pk);
+      }
+      float a0, a1, b0, b1;
+      f2_unpack(acc[0], a0, a1);
+      f2_unpack(acc[1], b0, b1);
+      l += (a0 + a1) + (b0 + b1);
+      // O rescale after the scores are dead (fewer live registers); it must land before
+      // p_full lets the next P.V product accumulate into O.
       if (__any_sync(0xffffffffu, fix_o)) {
         const float f = fix_o ? alpha : 1.f;
 #pragma unroll
@@ -345,21 +375,6 @@ __device__ bool softmax_role(const FwdArgs &a, FwdBars *bars, uint32_t tmem, int
           tmem_st16(tO + cc, o);
         }
       }
-      const float m_use = (m == NEG_INF) ? 0.f : m;
-      float rs = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < BN; cc += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(s[cc + 2 * e]), c, -m_use));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(s[cc + 2 * e + 1]), c, -m_use));
-          rs += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tS + cc / 2, pk);
-      }
-      l += rs;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
