@@ -100,12 +100,16 @@ namespace {
 // query rows for dQ) and stream 128-row tiles of the other side; every product is
 // 128 x 128 x 128 (K = 16 per instruction). Warp roles: 0-3 and 4-7 two softmax
 // warpgroups, warpgroup w owning columns [64 w, 64 w + 64) of every 128 x 128 score
-// tile (thread = row of the tile = TMEM lane); 8 TMA producer; 9 MMA issuer; 10-11
-// idle (3 warps per SM sub-partition: up to 168 registers per thread).
+// tile (thread = row of the tile = TMEM lane); 8 TMA producer; 9 MMA issuer; 10 a second
+// MMA issuer in the dQ kernel (one thread issuing back to back cannot keep the tensor
+// core busy while the softmax warps load the SM: each tcgen05.mma issue costs that thread
+// about as long as the product takes to run), idle in the dK/dV kernel; 11 idle (3 warps
+// per SM sub-partition: up to 168 registers per thread).
 constexpr int BW_WARPS = 12;
 constexpr int BW_THREADS = BW_WARPS * 32;
 constexpr int BW_PRODUCER = 8;
-constexpr int BW_MMA = 9;
+constexpr int BW_MMA = 9;       // MMA issuer (owns TMEM)
+constexpr int BW_MMA2 = 10;     // second MMA issuer of the dQ kernel
 constexpr int RT_BYTES = BM * 4;   // 128 row terms (int32 / fp32)
 
 __device__ __forceinline__ void load_tile(const CUtensorMap *m, uint64_t *bar, uint8_t *dst, int h, int row0, int b) {
@@ -192,7 +196,9 @@ __device__ __forceinline__ int range_tiles(const TileRange &R) { return R.empty(
 //   P^T  = exp2(S^T c - lse2) (masked)        -> bf16 over A (columns 16c .. 16c+7 of chunk c)
 //   dS^T = P^T (dP^T - delta)                 -> bf16 over B (the same columns of B)
 //   dV  += P^T . dO_j,  dK += dS^T . Q_j      (dK scaled by 1/sqrt(D) in the epilogue)
-// TMEM: A [0, 128), B [128, 256), dV [256, 384), dK [384, 512). Tensor-core order per
+// TMEM: A [0, 128), B [128, 256), dV [256, 384), dK [384, 512). One MMA issuer (warp 9):
+// a second one does not help here, because the P phase of tile j+1 needs S^T(j+1), which
+// needs region A back from dV(j), which needs the P phase of tile j. Tensor-core order per
 // tile: dV(j), S^T(j+1), dK(j), dP^T(j+1), so that the P phase of tile j+1 runs under
 // dK(j) and dP^T(j+1), and the dS phase of tile j under dV(j) and S^T(j+1).
 constexpr int KV_STAGE_BYTES = 2 * TILE_BYTES + 3 * RT_BYTES;   // Q, dO, lo, lse2, delta
@@ -566,9 +572,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 //   S    = Q . K_j^T  -> A_{j % 2}      dP = dO . V_j^T -> B
 //   P    = exp2(S c - lse2) (masked),  dS = P (dP - delta)  -> bf16 over A_{j % 2}
 //   dQ  += dS . K_j   (C; scaled by 1/sqrt(D) in the epilogue)
-// TMEM: A0 [0, 128), A1 [128, 256), B [256, 384), C [384, 512). Tensor-core order:
-// dQ(j), dP(j+1), S(j+2): the P phase of tile j+1 runs under dQ(j) and dP(j+1), its dS
-// phase under S(j+2). Deterministic: every dQ row is summed by one CTA in a fixed order.
+// TMEM: A0 [0, 128), A1 [128, 256), B [256, 384), C [384, 512). Two MMA issuers: warp
+// 9 runs S(j) (two tiles ahead) and dQ(j), warp 10 runs dP(j). Deterministic: every dQ
+// row is summed by one CTA in a fixed order.
 constexpr int DQ_KSTAGES = 3, DQ_VSTAGES = 2;
 constexpr int DQ_SM_Q = 0, DQ_SM_DO = TILE_BYTES, DQ_SM_K = 2 * TILE_BYTES;
 constexpr int DQ_SM_V = DQ_SM_K + DQ_KSTAGES * TILE_BYTES;
@@ -633,11 +639,15 @@ __device__ __forceinline__ bool dq_producer(const CUtensorMap *tq, const CUtenso
   return ok;
 }
 
-__device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *bars, uint32_t tmem, int lane) {
+// MMA chains of the dQ kernel. chain 0 (warp 9): S(j) = Q K_j^T into A_{j % 2} (two
+// ahead), dQ += dS(j) K_j once the softmax has written dS(j); chain 1 (warp 10): dP(j) =
+// dO V_j^T into B, each after the softmax has finished reading the previous dP.
+__device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *bars, uint32_t tmem, int chain,
+                                       int lane) {
   volatile int *abort = &bars->abort;
   const uint32_t q_s = smem_u32(smem + DQ_SM_Q), do_s = smem_u32(smem + DQ_SM_DO);
   const uint32_t k0_s = smem_u32(smem + DQ_SM_K), v0_s = smem_u32(smem + DQ_SM_V);
-  int k_use = 0, v_use = 0, own = 0;
+  int k_use = 0, v_use = 0, own = 0, dp_issued = 0;
   uint32_t dsf_par = 0, ae_par = 1;
   bool ok = true;
   for (int it = 0; ok; ++it) {
@@ -652,61 +662,65 @@ __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *b
     if (!(ok = mbar_wait(&bars->own_full, it & 1, abort))) break;
     ++own;
     tc_fence_after();
-    const int kb = k_use, vb = v_use;
-    auto k_s = [&](int j) { return k0_s + uint32_t((kb + j) % DQ_KSTAGES) * TILE_BYTES; };
-    auto v_s = [&](int j) { return v0_s + uint32_t((vb + j) % DQ_VSTAGES) * TILE_BYTES; };
-    auto issue_s = [&](int j) -> bool {   // S(j) = Q K_j^T into A_{j % 2}
-      if (!mbar_wait(&bars->k_full[(kb + j) % DQ_KSTAGES], ((kb + j) / DQ_KSTAGES) & 1, abort)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        mma_tile_kk(tmem + uint32_t(j & 1) * 128, q_s, k_s(j), false);
-        mma_commit(&bars->s_full[j & 1]);
+    if (chain == 0) {
+      const int kb = k_use;
+      auto k_s = [&](int j) { return k0_s + uint32_t((kb + j) % DQ_KSTAGES) * TILE_BYTES; };
+      auto issue_s = [&](int j) -> bool {   // S(j) = Q K_j^T into A_{j % 2}
+        if (!mbar_wait(&bars->k_full[(kb + j) % DQ_KSTAGES], ((kb + j) / DQ_KSTAGES) & 1, abort)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          mma_tile_kk(tmem + uint32_t(j & 1) * 128, q_s, k_s(j), false);
+          mma_commit(&bars->s_full[j & 1]);
+        }
+        __syncwarp();
+        return true;
+      };
+      if (n > 0) ok = issue_s(0) && (n < 2 || issue_s(1));
+      for (int j = 0; j < n && ok; ++j) {
+        if (!(ok = mbar_wait(&bars->ds_full, dsf_par, abort))) break;
+        dsf_par ^= 1;
+        if (j == 0) {
+          if (!(ok = mbar_wait(&bars->acc_empty, ae_par, abort))) break;
+          ae_par ^= 1;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          mma_tile_ts(tmem + DQ_COL_C, tmem + uint32_t(j & 1) * 128, k_s(j), j > 0);   // dQ += dS K
+          mma_commit(&bars->k_empty[(kb + j) % DQ_KSTAGES]);
+        }
+        __syncwarp();
+        if (j + 2 < n && !(ok = issue_s(j + 2))) break;   // A_{j % 2} is reused after dQ(j), in order
       }
-      __syncwarp();
-      return true;
-    };
-    auto issue_dp = [&](int j) -> bool {   // dP(j) = dO V_j^T into B; V_j is then released
-      if (!mbar_wait(&bars->v_full[(vb + j) % DQ_VSTAGES], ((vb + j) / DQ_VSTAGES) & 1, abort)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        mma_tile_kk(tmem + DQ_COL_B, do_s, v_s(j), false);
-        mma_commit(&bars->dp_full);
-        mma_commit(&bars->v_empty[(vb + j) % DQ_VSTAGES]);
+      if (!ok) break;
+      k_use = kb + n;
+      if (lane == 0 && n > 0) mma_commit(&bars->acc_full);
+    } else {
+      for (int j = 0; j < n && ok; ++j, ++v_use) {
+        const int vs = v_use % DQ_VSTAGES;
+        if (!(ok = mbar_wait(&bars->v_full[vs], (v_use / DQ_VSTAGES) & 1, abort))) break;
+        if (dp_issued > 0) {   // B still holds the previous dP until its dS phase is done
+          if (!(ok = mbar_wait(&bars->ds_full, dsf_par, abort))) break;
+          dsf_par ^= 1;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          mma_tile_kk(tmem + DQ_COL_B, do_s, v0_s + uint32_t(vs) * TILE_BYTES, false);   // dP = dO V^T
+          mma_commit(&bars->dp_full);
+          mma_commit(&bars->v_empty[vs]);
+        }
+        __syncwarp();
+        ++dp_issued;
       }
-      __syncwarp();
-      return true;
-    };
-    if (n > 0) ok = issue_s(0) && issue_dp(0) && (n < 2 || issue_s(1));
-    for (int j = 0; j < n && ok; ++j) {
-      if (!(ok = mbar_wait(&bars->ds_full, dsf_par, abort))) break;
-      dsf_par ^= 1;
-      if (j == 0) {
-        if (!(ok = mbar_wait(&bars->acc_empty, ae_par, abort))) break;
-        ae_par ^= 1;
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        mma_tile_ts(tmem + DQ_COL_C, tmem + uint32_t(j & 1) * 128, k_s(j), j > 0);   // dQ += dS K
-        mma_commit(&bars->k_empty[(kb + j) % DQ_KSTAGES]);
-      }
-      __syncwarp();
-      if (j + 1 < n && !(ok = issue_dp(j + 1))) break;
-      if (j + 2 < n && !(ok = issue_s(j + 2))) break;
+      if (!ok) break;
     }
-    if (!ok) break;
-    k_use = kb + n;
-    v_use = vb + n;
-    if (lane == 0) {
-      if (n > 0) mma_commit(&bars->acc_full);
-      mma_commit(&bars->own_empty);
-    }
+    if (lane == 0) mma_commit(&bars->own_empty);
     __syncwarp();
   }
-  if (lane == 0) {
+  if (lane == 0 && chain == 0) {
     bars->k_use = k_use;
-    bars->v_use = v_use;
     bars->own_used = own;
   }
+  if (lane == 0 && chain == 1) bars->v_use = v_use;
   return ok;
 }
 
@@ -749,13 +763,20 @@ __device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32
       sf_par[j & 1] ^= 1;
       tc_fence_after();
       float p[64];
+      uint32_t sv[64];
+      tmem_ld16(tA, sv);
+      tmem_ld16(tA + 16, sv + 16);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        uint32_t sv[16];
-        tmem_ld16(tA + ch * 16, sv);
-        tmem_ld_wait();
+        if (ch == 0 || ch == 2) {
+          tmem_ld_wait();
+          if (ch == 0) {
+            tmem_ld16(tA + 32, sv + 32);
+            tmem_ld16(tA + 48, sv + 48);
+          }
+        }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) p[ch * 16 + e] = ex2_approx(fmaf(__uint_as_float(sv[e]), c, -l2));
+        for (int e = 0; e < 16; ++e) p[ch * 16 + e] = ex2_approx(fmaf(__uint_as_float(sv[ch * 16 + e]), c, -l2));
         if (!full) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -769,16 +790,23 @@ __device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32
       if (!(ok = mbar_wait(&bars->dp_full, dpf_par, abort))) break;
       dpf_par ^= 1;
       tc_fence_after();
+      uint32_t dv[64];
+      tmem_ld16(tB, dv);
+      tmem_ld16(tB + 16, dv + 16);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        uint32_t dv[16];
-        tmem_ld16(tB + ch * 16, dv);
-        tmem_ld_wait();
+        if (ch == 0 || ch == 2) {
+          tmem_ld_wait();
+          if (ch == 0) {
+            tmem_ld16(tB + 32, dv + 32);
+            tmem_ld16(tB + 48, dv + 48);
+          }
+        }
         uint32_t dk[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          dk[e] = pack_bf16x2(p[ch * 16 + 2 * e] * (__uint_as_float(dv[2 * e]) - dl),
-                              p[ch * 16 + 2 * e + 1] * (__uint_as_float(dv[2 * e + 1]) - dl));
+          dk[e] = pack_bf16x2(p[ch * 16 + 2 * e] * (__uint_as_float(dv[ch * 16 + 2 * e]) - dl),
+                              p[ch * 16 + 2 * e + 1] * (__uint_as_float(dv[ch * 16 + 2 * e + 1]) - dl));
         tmem_st8(tA + ch * 16, dk);
       }
       tmem_st_wait();
@@ -824,15 +852,15 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->item_full[s], 1);
-      mbar_init(&bars->item_empty[s], 9);   // softmax 8 + MMA 1 warps
+      mbar_init(&bars->item_empty[s], 10);  // softmax 8 + MMA 2 warps
     }
     mbar_init(&bars->own_full, 1);
-    mbar_init(&bars->own_empty, 1);
+    mbar_init(&bars->own_empty, 2);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->ds_full, 8);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 2);
     bars->abort = 0;
     bars->k_fill = bars->k_use = bars->v_fill = bars->v_use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
@@ -857,8 +885,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   } else if (warp == BW_PRODUCER) {
     if (lane == 0) ok = dq_producer(&tq, &tk, &tv, &tdo, a, smem, bars);
     __syncwarp();
-  } else if (warp == BW_MMA) {
-    ok = dq_mma(a, smem, bars, tmem, lane);
+  } else if (warp == BW_MMA || warp == BW_MMA2) {
+    ok = dq_mma(a, smem, bars, tmem, warp - BW_MMA, lane);
   }
 
   if (!ok) {
@@ -875,7 +903,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         bounded_wait_plain_bw(&bars->v_full[k % DQ_VSTAGES], (k / DQ_VSTAGES) & 1);
       if (bars->own_issued > bars->own_used) bounded_wait_plain_bw(&bars->own_full, (bars->own_issued - 1) & 1);
     }
-    if (warp == BW_MMA && lane == 0) {
+    if ((warp == BW_MMA || warp == BW_MMA2) && lane == 0) {
       mma_commit(&bars->drain);
       bounded_wait_plain_bw(&bars->drain, 0);
     }

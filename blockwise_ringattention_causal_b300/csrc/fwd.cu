@@ -14,12 +14,13 @@
 //   warps 0-3  softmax for query tile 0 (one TMEM lane = one query row per thread)
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer (and the scheduler ticket)
-//   warp  9    tcgen05 MMA issuer (and TMEM owner)
-//   warps 10-11 idle (they keep 3 warps per SM sub-partition)
+//   warp  9    tcgen05 MMA issuer of query tile 0 (and TMEM owner)
+//   warp  10   tcgen05 MMA issuer of query tile 1
+//   warp  11   idle (it keeps 3 warps per SM sub-partition)
 // TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P (bf16) is written
-// over the first 64 columns of its S. MMA order per key tile j:
-//   S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
-// so that one softmax warpgroup works while the tensor core serves the other.
+// over the first 64 columns of its S. Each MMA issuer runs S_t(j), PV_t(j-1) ... for
+// its own query tile, so one softmax warpgroup works while the tensor core serves the
+// other.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -29,7 +30,8 @@ namespace {
 constexpr int FWD_WARPS = 12;   // 3 warps per SM sub-partition: 168 registers each
 constexpr int FWD_THREADS = FWD_WARPS * 32;
 constexpr int WARP_PRODUCER = 8;
-constexpr int WARP_MMA = 9;
+constexpr int WARP_MMA = 9;    // MMA issuer of query tile 0 (and TMEM owner)
+constexpr int WARP_MMA2 = 10;  // MMA issuer of query tile 1
 constexpr int KV_STAGES = 4;
 
 constexpr int SM_Q = 0;
@@ -165,23 +167,22 @@ __device__ bool producer_role(const CUtensorMap *tq, const CUtensorMap *tk, cons
   return ok;
 }
 
-// ----------------------------------------------------------------------------- MMA issuer
-__device__ bool mma_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_t tmem, int kv_chunk,
+// ----------------------------------------------------------------------------- MMA issuers
+// Chain t (warp 9 for query tile 0, warp 10 for query tile 1): per key tile in ring
+// order, P.V of the previous key tile (once the softmax has written its P), then
+// S_t = Q_t K^T of this one into the same TMEM columns (the tensor core runs one
+// thread's products in order). Two issuing threads keep the tensor core busy where one
+// could not: each tcgen05.mma issue costs the issuing thread about as long as the
+// product takes to run. A K or V stage is released when both chains are done with it
+// (a chain whose tile does not see a key tile releases its stages at once).
+__device__ bool mma_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_t tmem, int kv_chunk, int t,
                          int lane) {
   volatile int *abort = &bars->abort;
-  const uint32_t q_s[2] = {smem_u32(smem + SM_Q), smem_u32(smem + SM_Q + TILE_BYTES)};
+  const uint32_t q_s = smem_u32(smem + SM_Q + t * TILE_BYTES);
   const uint32_t kv_s0 = smem_u32(smem + SM_KV);
   int kv_use = 0, q_used = 0;
-  uint32_t pf_par[2] = {0, 0}, oe_par[2] = {1, 1};
+  uint32_t pf_par = 0, oe_par = 1;
   bool ok = true;
-
-  auto wait_kv = [&](int &st) -> bool {
-    st = kv_use % KV_STAGES;
-    const bool r = mbar_wait(&bars->kv_full[st], (kv_use / KV_STAGES) & 1, abort);
-    ++kv_use;
-    tc_fence_after();
-    return r;
-  };
 
   for (int it = 0;; ++it) {
     const int slot = it & 1;
@@ -192,72 +193,77 @@ __device__ bool mma_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_
     if (item < 0) break;
     const Item I = decode(a, item);
     const Ranges R = item_ranges(a, I);
+    const TileRange my = R.r[t];
     if (!(ok = mbar_wait(&bars->q_full, it & 1, abort))) break;
     ++q_used;
     tc_fence_after();
-    bool first[2] = {true, true};
+    bool first = true;
+    int prev_v = -1;   // stage of the V tile whose P.V product is still to be issued
     KvSeq seq;
-    seq.init(R.first, R.last, kv_chunk);
-    if (seq.valid()) {
-      int stK;
-      if (!(ok = wait_kv(stK))) break;
+    for (seq.init(R.first, R.last, kv_chunk); seq.valid() && ok; seq.next()) {
+      const int stK = kv_use % KV_STAGES, parK = (kv_use / KV_STAGES) & 1;
+      const int stV = (kv_use + 1) % KV_STAGES, parV = ((kv_use + 1) / KV_STAGES) & 1;
+      kv_use += 2;
+      if (!(ok = mbar_wait(&bars->kv_full[stK], parK, abort))) break;
+      tc_fence_after();
+      if (!my.has(seq.t)) {
+        // this query tile sees no key of the tile: release K and V (after they have
+        // arrived, so that the arrivals count for this use of the stages)
+        if (!(ok = mbar_wait(&bars->kv_full[stV], parV, abort))) break;
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->kv_empty[stK]);
+          mbar_arrive(&bars->kv_empty[stV]);
+        }
+        __syncwarp();
+        continue;
+      }
+      if (prev_v >= 0) {
+        if (first) {
+          if (!(ok = mbar_wait(&bars->o_empty[t], oe_par, abort))) break;
+          oe_par ^= 1;
+        }
+        if (!(ok = mbar_wait(&bars->p_full[t], pf_par, abort))) break;
+        pf_par ^= 1;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_pv(tmem + col_o(t), tmem + col_s(t), kv_s0 + prev_v * TILE_BYTES, !first);
+          mma_commit(&bars->kv_empty[prev_v]);
+        }
+        first = false;
+      }
       if (lane == 0) {
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (R.r[t].has(seq.t)) {
-            issue_qk(tmem + col_s(t), q_s[t], kv_s0 + stK * TILE_BYTES);
-            mma_commit(&bars->s_full[t]);
-          }
+        issue_qk(tmem + col_s(t), q_s, kv_s0 + stK * TILE_BYTES);
+        mma_commit(&bars->s_full[t]);
         mma_commit(&bars->kv_empty[stK]);
       }
       __syncwarp();
-      while (ok) {
-        const int cur = seq.t;
-        int stV;
-        if (!(ok = wait_kv(stV))) break;
-        seq.next();
-        const bool has_next = seq.valid();
-        const int nxt = seq.t;
-        int stK2 = -1;
-#pragma unroll
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (R.r[t].has(cur)) {
-            if (first[t]) {
-              if (!(ok = mbar_wait(&bars->o_empty[t], oe_par[t], abort))) break;
-              oe_par[t] ^= 1;
-            }
-            if (!(ok = mbar_wait(&bars->p_full[t], pf_par[t], abort))) break;
-            pf_par[t] ^= 1;
-            tc_fence_after();
-            if (lane == 0) issue_pv(tmem + col_o(t), tmem + col_s(t), kv_s0 + stV * TILE_BYTES, !first[t]);
-            first[t] = false;
-          }
-          // V(cur) is free once both P.V products are done: release it before S1(next)
-          // is queued, so that the producer can refill its stage half a step earlier.
-          if (t == 1 && lane == 0) mma_commit(&bars->kv_empty[stV]);
-          if (has_next) {
-            if (t == 0 && !(ok = wait_kv(stK2))) break;
-            if (lane == 0 && R.r[t].has(nxt)) {
-              issue_qk(tmem + col_s(t), q_s[t], kv_s0 + stK2 * TILE_BYTES);
-              mma_commit(&bars->s_full[t]);
-            }
-          }
-        }
-        if (!ok) break;
-        if (lane == 0 && has_next) mma_commit(&bars->kv_empty[stK2]);
-        __syncwarp();
-        if (!has_next) break;
+      // V of this key tile: its P.V product comes with the next key tile (or below)
+      if (!(ok = mbar_wait(&bars->kv_full[stV], parV, abort))) break;
+      prev_v = stV;
+    }
+    if (!ok) break;
+    if (prev_v >= 0) {
+      if (first) {
+        if (!(ok = mbar_wait(&bars->o_empty[t], oe_par, abort))) break;
+        oe_par ^= 1;
       }
-      if (!ok) break;
+      if (!(ok = mbar_wait(&bars->p_full[t], pf_par, abort))) break;
+      pf_par ^= 1;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_pv(tmem + col_o(t), tmem + col_s(t), kv_s0 + prev_v * TILE_BYTES, !first);
+        mma_commit(&bars->kv_empty[prev_v]);
+      }
+      first = false;
     }
     if (lane == 0) {
       mma_commit(&bars->q_empty);
-      if (!first[0]) mma_commit(&bars->o_full[0]);
-      if (!first[1]) mma_commit(&bars->o_full[1]);
+      if (!first) mma_commit(&bars->o_full[t]);
     }
     __syncwarp();
   }
-  if (lane == 0) {
+  if (lane == 0 && t == 0) {
     bars->kv_use = kv_use;
     bars->q_used = q_used;
   }
@@ -438,19 +444,19 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < KV_STAGES; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->kv_empty[s], 2);   // both MMA chains
     }
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->q_empty, 2);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 4);
       mbar_init(&bars->o_full[t], 1);
       mbar_init(&bars->o_empty[t], 4);
       mbar_init(&bars->item_full[t], 1);
-      mbar_init(&bars->item_empty[t], 9);
+      mbar_init(&bars->item_empty[t], 10);   // softmax 8 + MMA 2 warps
     }
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 2);
     bars->abort = 0;
     bars->kv_fill = bars->kv_use = bars->q_issued = bars->q_used = 0;
     fence_mbar_init();
@@ -473,8 +479,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   if (warp == WARP_PRODUCER) {
     if (lane == 0) ok = producer_role(&tq, &tk, &tv, a, smem, bars, kv_chunk);
     __syncwarp();
-  } else if (warp == WARP_MMA) {
-    ok = mma_role(a, smem, bars, tmem, kv_chunk, lane);
+  } else if (warp == WARP_MMA || warp == WARP_MMA2) {
+    ok = mma_role(a, smem, bars, tmem, kv_chunk, warp - WARP_MMA, lane);
   } else if (warp < 8) {
     ok = softmax_role(a, bars, tmem, kv_chunk, warp >> 2, warp, lane);
   }
@@ -491,7 +497,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         bounded_wait_plain(&bars->kv_full[n % KV_STAGES], (n / KV_STAGES) & 1);
       if (bars->q_issued > bars->q_used) bounded_wait_plain(&bars->q_full, (bars->q_issued - 1) & 1);
     }
-    if (warp == WARP_MMA && lane == 0) {
+    if ((warp == WARP_MMA || warp == WARP_MMA2) && lane == 0) {
       mma_commit(&bars->drain);
       bounded_wait_plain(&bars->drain, 0);
     }
