@@ -14,13 +14,15 @@
 //   warps 0-3  softmax for query tile 0 (one TMEM lane = one query row per thread)
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer (and the scheduler ticket)
-//   warp  9    tcgen05 MMA issuer of query tile 0 (and TMEM owner)
-//   warp  10   tcgen05 MMA issuer of query tile 1
+//   warp  9    tcgen05 issuer of the S = Q K^T products (and TMEM owner)
+//   warp  10   tcgen05 issuer of the O += P V products
 //   warp  11   idle (it keeps 3 warps per SM sub-partition)
-// TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P (bf16) is written
-// over the first 64 columns of its S. Each MMA issuer runs S_t(j), PV_t(j-1) ... for
-// its own query tile, so one softmax warpgroup works while the tensor core serves the
-// other.
+// TMEM (512 columns): S (128 fp32 columns, shared by the two query tiles in turn) |
+// P0 | P1 (64 columns each, bf16 pairs) | O0 | O1 (128 fp32 columns each). Because P
+// has columns of its own, the S product of the next key tile does not wait for the P.V
+// product of this one: it only needs the other tile's softmax to have read S out of
+// TMEM, which it does first. So S(j+1) runs while the softmax still works on tile j,
+// and the tensor core interleaves S0, S1, P0.V and P1.V products.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -30,8 +32,8 @@ namespace {
 constexpr int FWD_WARPS = 12;   // 3 warps per SM sub-partition: 168 registers each
 constexpr int FWD_THREADS = FWD_WARPS * 32;
 constexpr int WARP_PRODUCER = 8;
-constexpr int WARP_MMA = 9;    // MMA issuer of query tile 0 (and TMEM owner)
-constexpr int WARP_MMA2 = 10;  // MMA issuer of query tile 1
+constexpr int WARP_MMA = 9;    // issuer of the S products (and TMEM owner)
+constexpr int WARP_MMA2 = 10;  // issuer of the P.V products
 constexpr int KV_STAGES = 4;
 
 constexpr int SM_Q = 0;
@@ -41,18 +43,19 @@ constexpr int SM_BAR = SM_KV + KV_STAGES * TILE_BYTES;
 struct FwdBars {
   uint64_t kv_full[KV_STAGES], kv_empty[KV_STAGES];
   uint64_t q_full, q_empty;
-  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t s_full[2], s_free, p_full[2], pv_done[2], o_empty[2];
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   int item[2];
   uint32_t tmem_base;
   int abort;
-  int kv_fill, kv_use, q_issued, q_used;
+  int kv_fill, kv_use_k, kv_use_v, q_issued, q_used;
 };
 
 constexpr int FWD_SMEM = SM_BAR + int(sizeof(FwdBars)) + 1024;   // + alignment slack
 
-__device__ __forceinline__ uint32_t col_s(int t) { return t ? 128u : 0u; }   // S_t (and P_t)
+constexpr uint32_t COL_S = 0;                                                  // S (either tile)
+__device__ __forceinline__ uint32_t col_p(int t) { return t ? 192u : 128u; }  // P_t
 __device__ __forceinline__ uint32_t col_o(int t) { return t ? 384u : 256u; }  // O_t
 constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);   // Q, K both K-major
 constexpr uint32_t IDESC_PV = idesc_bf16(BM, HD, false, true);    // P from TMEM, V MN-major
@@ -168,22 +171,19 @@ __device__ bool producer_role(const CUtensorMap *tq, const CUtensorMap *tk, cons
 }
 
 // ----------------------------------------------------------------------------- MMA issuers
-// Chain t (warp 9 for query tile 0, warp 10 for query tile 1): per key tile in ring
-// order, P.V of the previous key tile (once the softmax has written its P), then
-// S_t = Q_t K^T of this one into the same TMEM columns (the tensor core runs one
-// thread's products in order). Two issuing threads keep the tensor core busy where one
-// could not: each tcgen05.mma issue costs the issuing thread about as long as the
-// product takes to run. A K or V stage is released when both chains are done with it
-// (a chain whose tile does not see a key tile releases its stages at once).
-__device__ bool mma_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_t tmem, int kv_chunk, int t,
-                         int lane) {
+// Two issuing threads keep the tensor core busy where one could not: each tcgen05.mma
+// issue costs the issuing thread about as long as the product takes to run.
+//
+// S issuer: per key tile in ring order, S_0 then S_1 (each only for a query tile that
+// sees the key tile) into the shared S columns, each once the softmax that read the
+// previous S has signalled s_free. Releases the K stage after its products and the Q
+// tiles after the item's last product.
+__device__ bool s_issuer_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_t tmem, int kv_chunk,
+                              int lane) {
   volatile int *abort = &bars->abort;
-  const uint32_t q_s = smem_u32(smem + SM_Q + t * TILE_BYTES);
   const uint32_t kv_s0 = smem_u32(smem + SM_KV);
-  int kv_use = 0, q_used = 0;
-  uint32_t pf_par = 0, oe_par = 1;
+  int kv_use = 0, q_used = 0, n_s = 0;
   bool ok = true;
-
   for (int it = 0;; ++it) {
     const int slot = it & 1;
     if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
@@ -193,80 +193,100 @@ __device__ bool mma_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_
     if (item < 0) break;
     const Item I = decode(a, item);
     const Ranges R = item_ranges(a, I);
-    const TileRange my = R.r[t];
     if (!(ok = mbar_wait(&bars->q_full, it & 1, abort))) break;
     ++q_used;
-    tc_fence_after();
-    bool first = true;
-    int prev_v = -1;   // stage of the V tile whose P.V product is still to be issued
     KvSeq seq;
     for (seq.init(R.first, R.last, kv_chunk); seq.valid() && ok; seq.next()) {
       const int stK = kv_use % KV_STAGES, parK = (kv_use / KV_STAGES) & 1;
-      const int stV = (kv_use + 1) % KV_STAGES, parV = ((kv_use + 1) / KV_STAGES) & 1;
-      kv_use += 2;
       if (!(ok = mbar_wait(&bars->kv_full[stK], parK, abort))) break;
-      tc_fence_after();
-      if (!my.has(seq.t)) {
-        // this query tile sees no key of the tile: release K and V (after they have
-        // arrived, so that the arrivals count for this use of the stages)
-        if (!(ok = mbar_wait(&bars->kv_full[stV], parV, abort))) break;
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars->kv_empty[stK]);
-          mbar_arrive(&bars->kv_empty[stV]);
-        }
-        __syncwarp();
-        continue;
-      }
-      if (prev_v >= 0) {
-        if (first) {
-          if (!(ok = mbar_wait(&bars->o_empty[t], oe_par, abort))) break;
-          oe_par ^= 1;
-        }
-        if (!(ok = mbar_wait(&bars->p_full[t], pf_par, abort))) break;
-        pf_par ^= 1;
+      kv_use += 2;
+      bool used = false;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (!R.r[t].has(seq.t)) continue;
+        // the S columns are free once the softmax of the previous S has read them
+        if (n_s > 0 && !(ok = mbar_wait(&bars->s_free, (n_s - 1) & 1, abort))) break;
         tc_fence_after();
         if (lane == 0) {
-          issue_pv(tmem + col_o(t), tmem + col_s(t), kv_s0 + prev_v * TILE_BYTES, !first);
-          mma_commit(&bars->kv_empty[prev_v]);
+          issue_qk(tmem + COL_S, smem_u32(smem + SM_Q + t * TILE_BYTES), kv_s0 + stK * TILE_BYTES);
+          mma_commit(&bars->s_full[t]);
         }
-        first = false;
+        __syncwarp();
+        ++n_s;
+        used = true;
       }
+      if (!ok) break;
       if (lane == 0) {
-        issue_qk(tmem + col_s(t), q_s, kv_s0 + stK * TILE_BYTES);
-        mma_commit(&bars->s_full[t]);
-        mma_commit(&bars->kv_empty[stK]);
+        if (used) mma_commit(&bars->kv_empty[stK]);
+        else mbar_arrive(&bars->kv_empty[stK]);
       }
       __syncwarp();
-      // V of this key tile: its P.V product comes with the next key tile (or below)
-      if (!(ok = mbar_wait(&bars->kv_full[stV], parV, abort))) break;
-      prev_v = stV;
     }
     if (!ok) break;
-    if (prev_v >= 0) {
-      if (first) {
-        if (!(ok = mbar_wait(&bars->o_empty[t], oe_par, abort))) break;
-        oe_par ^= 1;
-      }
-      if (!(ok = mbar_wait(&bars->p_full[t], pf_par, abort))) break;
-      pf_par ^= 1;
-      tc_fence_after();
-      if (lane == 0) {
-        issue_pv(tmem + col_o(t), tmem + col_s(t), kv_s0 + prev_v * TILE_BYTES, !first);
-        mma_commit(&bars->kv_empty[prev_v]);
-      }
-      first = false;
-    }
-    if (lane == 0) {
-      mma_commit(&bars->q_empty);
-      if (!first) mma_commit(&bars->o_full[t]);
-    }
+    if (lane == 0) mma_commit(&bars->q_empty);
     __syncwarp();
   }
-  if (lane == 0 && t == 0) {
-    bars->kv_use = kv_use;
+  if (lane == 0) {
+    bars->kv_use_k = kv_use;
     bars->q_used = q_used;
   }
+  return ok;
+}
+
+// P.V issuer: per key tile in ring order, O_0 += P_0 V then O_1 += P_1 V (each once its
+// softmax has written P_t and rescaled O_t), then releases the V stage. The first
+// product of an item overwrites O_t once the previous item's O_t has been read out.
+__device__ bool pv_issuer_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_t tmem, int kv_chunk,
+                               int lane) {
+  volatile int *abort = &bars->abort;
+  const uint32_t kv_s0 = smem_u32(smem + SM_KV);
+  int kv_use = 0;
+  uint32_t pf_par[2] = {0, 0}, oe_par[2] = {1, 1};
+  bool ok = true;
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
+    const int item = bars->item[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+    if (item < 0) break;
+    const Item I = decode(a, item);
+    const Ranges R = item_ranges(a, I);
+    bool first[2] = {true, true};
+    KvSeq seq;
+    for (seq.init(R.first, R.last, kv_chunk); seq.valid() && ok; seq.next()) {
+      const int stV = (kv_use + 1) % KV_STAGES, parV = ((kv_use + 1) / KV_STAGES) & 1;
+      if (!(ok = mbar_wait(&bars->kv_full[stV], parV, abort))) break;
+      kv_use += 2;
+      bool used = false;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (!R.r[t].has(seq.t)) continue;
+        if (first[t]) {
+          if (!(ok = mbar_wait(&bars->o_empty[t], oe_par[t], abort))) break;
+          oe_par[t] ^= 1;
+        }
+        if (!(ok = mbar_wait(&bars->p_full[t], pf_par[t], abort))) break;
+        pf_par[t] ^= 1;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_pv(tmem + col_o(t), tmem + col_p(t), kv_s0 + stV * TILE_BYTES, !first[t]);
+          mma_commit(&bars->pv_done[t]);
+        }
+        __syncwarp();
+        first[t] = false;
+        used = true;
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        if (used) mma_commit(&bars->kv_empty[stV]);
+        else mbar_arrive(&bars->kv_empty[stV]);
+      }
+      __syncwarp();
+    }
+    if (!ok) break;
+  }
+  if (lane == 0) bars->kv_use_v = kv_use;
   return ok;
 }
 
@@ -277,10 +297,11 @@ __device__ bool softmax_role(const FwdArgs &a, FwdBars *bars, uint32_t tmem, int
   const int wq = warp & 3;
   const int r = wq * 32 + lane;
   const uint32_t lane_off = uint32_t(wq * 32) << 16;
-  const uint32_t tS = tmem + lane_off + col_s(t);
+  const uint32_t tS = tmem + lane_off + COL_S;
+  const uint32_t tP = tmem + lane_off + col_p(t);
   const uint32_t tO = tmem + lane_off + col_o(t);
   const float c = a.scale_log2;
-  uint32_t sf_par = 0, of_par = 0;
+  uint32_t sf_par = 0, pd_par = 0;
   bool ok = true;
 
   for (int it = 0;; ++it) {
@@ -315,6 +336,10 @@ __device__ bool softmax_role(const FwdArgs &a, FwdBars *bars, uint32_t tmem, int
       tmem_ld32(tS + 64, s + 64);
       tmem_ld32(tS + 96, s + 96);
       tmem_ld_wait();
+      // S is in registers: the S columns may take the next product
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_free);
       const int k0 = kt * BN;
       const bool full = (lo_qb <= k0) && (k0 + BN - 1 <= q0);
       if (!full) {
@@ -346,27 +371,30 @@ __device__ bool softmax_role(const FwdArgs &a, FwdBars *bars, uint32_t tmem, int
       const bool fix_o = resc && had && l > 0.f;
       l *= alpha;
       const float m_use = (m == NEG_INF) ? 0.f : m;
-      // p = exp2(s c - m) two at a time (paired fma and add), P written back as bf16
+      // p = exp2(s c - m) two at a time (paired fma and add), packed to bf16 pairs
       const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_use, -m_use);
       uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+      uint32_t pk[BN / 2];
 #pragma unroll
-      for (int cc = 0; cc < BN; cc += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[cc + 2 * e]), __uint_as_float(s[cc + 2 * e + 1])), c2, nm2), x0,
-                    x1);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          acc[e & 1] = f2_add(acc[e & 1], f2_pack(p0, p1));
-          pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tS + cc / 2, pk);
+      for (int e = 0; e < BN / 2; ++e) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), c2, nm2), x0, x1);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        acc[e & 1] = f2_add(acc[e & 1], f2_pack(p0, p1));
+        pk[e] = pack_bf16x2(p0, p1);
       }
       float a0, a1, b0, b1;
       f2_unpack(acc[0], a0, a1);
       f2_unpack(acc[1], b0, b1);
       l += (a0 + a1) + (b0 + b1);
+      // P_t and O_t belong to the previous P.V product until it completes
+      if (had) {
+        if (!(ok = mbar_wait(&bars->pv_done[t], pd_par, abort))) break;
+        pd_par ^= 1;
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int cc = 0; cc < BN / 2; cc += 16) tmem_st16(tP + cc, pk + cc);
       // O rescale after the scores are dead (fewer live registers); it must land before
       // p_full lets the next P.V product accumulate into O.
       if (__any_sync(0xffffffffu, fix_o)) {
@@ -391,8 +419,8 @@ __device__ bool softmax_role(const FwdArgs &a, FwdBars *bars, uint32_t tmem, int
 
     const size_t orow = (size_t(I.b) * a.S + i) * a.H + I.h;
     if (had) {
-      if (!(ok = mbar_wait(&bars->o_full[t], of_par, abort))) break;
-      of_par ^= 1;
+      if (!(ok = mbar_wait(&bars->pv_done[t], pd_par, abort))) break;
+      pd_par ^= 1;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
@@ -444,21 +472,22 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < KV_STAGES; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 2);   // both MMA chains
+      mbar_init(&bars->kv_empty[s], 1);   // K stages: the S issuer; V stages: the P.V issuer
     }
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 2);
+    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->s_free, 4);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 4);
-      mbar_init(&bars->o_full[t], 1);
+      mbar_init(&bars->pv_done[t], 1);
       mbar_init(&bars->o_empty[t], 4);
       mbar_init(&bars->item_full[t], 1);
       mbar_init(&bars->item_empty[t], 10);   // softmax 8 + MMA 2 warps
     }
     mbar_init(&bars->drain, 2);
     bars->abort = 0;
-    bars->kv_fill = bars->kv_use = bars->q_issued = bars->q_used = 0;
+    bars->kv_fill = bars->kv_use_k = bars->kv_use_v = bars->q_issued = bars->q_used = 0;
     fence_mbar_init();
   }
   if (warp == WARP_MMA) {
@@ -479,8 +508,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   if (warp == WARP_PRODUCER) {
     if (lane == 0) ok = producer_role(&tq, &tk, &tv, a, smem, bars, kv_chunk);
     __syncwarp();
-  } else if (warp == WARP_MMA || warp == WARP_MMA2) {
-    ok = mma_role(a, smem, bars, tmem, kv_chunk, warp - WARP_MMA, lane);
+  } else if (warp == WARP_MMA) {
+    ok = s_issuer_role(a, smem, bars, tmem, kv_chunk, lane);
+  } else if (warp == WARP_MMA2) {
+    ok = pv_issuer_role(a, smem, bars, tmem, kv_chunk, lane);
   } else if (warp < 8) {
     ok = softmax_role(a, bars, tmem, kv_chunk, warp >> 2, warp, lane);
   }
@@ -493,8 +524,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   if (bars->abort) {
     // Let copies and MMAs still in flight land before shared memory and TMEM go away.
     if (warp == WARP_PRODUCER && lane == 0) {
-      for (int n = bars->kv_use; n < bars->kv_fill; ++n)
-        bounded_wait_plain(&bars->kv_full[n % KV_STAGES], (n / KV_STAGES) & 1);
+      // loads no consumer has waited for: K (even n) from the S issuer's count, V (odd n)
+      // from the P.V issuer's
+      for (int n = min(bars->kv_use_k, bars->kv_use_v); n < bars->kv_fill; ++n)
+        if (n >= ((n & 1) ? bars->kv_use_v : bars->kv_use_k))
+          bounded_wait_plain(&bars->kv_full[n % KV_STAGES], (n / KV_STAGES) & 1);
       if (bars->q_issued > bars->q_used) bounded_wait_plain(&bars->q_full, (bars->q_issued - 1) & 1);
     }
     if ((warp == WARP_MMA || warp == WARP_MMA2) && lane == 0) {
