@@ -100,16 +100,16 @@ namespace {
 // query rows for dQ) and stream 128-row tiles of the other side; every product is
 // 128 x 128 x 128 (K = 16 per instruction). Warp roles: 0-3 and 4-7 two softmax
 // warpgroups, warpgroup w owning columns [64 w, 64 w + 64) of every 128 x 128 score
-// tile (thread = row of the tile = TMEM lane); 8 TMA producer; 9 MMA issuer; 10 a second
-// MMA issuer in the dQ kernel (one thread issuing back to back cannot keep the tensor
-// core busy while the softmax warps load the SM: each tcgen05.mma issue costs that thread
-// about as long as the product takes to run), idle in the dK/dV kernel; 11 idle (3 warps
-// per SM sub-partition: up to 168 registers per thread).
+// tile (thread = row of the tile = TMEM lane); 8 TMA producer; 9 and 10 two MMA issuers
+// (one thread issuing back to back cannot keep the tensor core busy while the softmax
+// warps load the SM: each tcgen05.mma issue costs that thread about as long as the
+// product takes to run); 11 idle (3 warps per SM sub-partition: up to 168 registers per
+// thread).
 constexpr int BW_WARPS = 12;
 constexpr int BW_THREADS = BW_WARPS * 32;
 constexpr int BW_PRODUCER = 8;
 constexpr int BW_MMA = 9;       // MMA issuer (owns TMEM)
-constexpr int BW_MMA2 = 10;     // second MMA issuer of the dQ kernel
+constexpr int BW_MMA2 = 10;     // second MMA issuer
 constexpr int RT_BYTES = BM * 4;   // 128 row terms (int32 / fp32)
 
 __device__ __forceinline__ void load_tile(const CUtensorMap *m, uint64_t *bar, uint8_t *dst, int h, int row0, int b) {
@@ -192,25 +192,27 @@ __device__ __forceinline__ int range_tiles(const TileRange &R) { return R.empty(
 // ============================================================================= dK/dV
 // Item: (b, h, key tile). Resident: K and V. Streamed: Q_j, dO_j and the rows' lo /
 // lse2 / delta terms (two stages). Per query tile j:
-//   S^T  = K . Q_j^T  -> A           dP^T = V . dO_j^T -> B
-//   P^T  = exp2(S^T c - lse2) (masked)        -> bf16 over A (columns 16c .. 16c+7 of chunk c)
-//   dS^T = P^T (dP^T - delta)                 -> bf16 over B (the same columns of B)
+//   S^T  = K . Q_j^T  -> X           dP^T = V . dO_j^T -> X (after S^T has been read)
+//   P^T  = exp2(S^T c - lse2) (masked)        -> bf16 in PT
+//   dS^T = P^T (dP^T - delta)                 -> bf16 in DS
 //   dV  += P^T . dO_j,  dK += dS^T . Q_j      (dK scaled by 1/sqrt(D) in the epilogue)
-// TMEM: A [0, 128), B [128, 256), dV [256, 384), dK [384, 512). One MMA issuer (warp 9):
-// a second one does not help here, because the P phase of tile j+1 needs S^T(j+1), which
-// needs region A back from dV(j), which needs the P phase of tile j. Tensor-core order per
-// tile: dV(j), S^T(j+1), dK(j), dP^T(j+1), so that the P phase of tile j+1 runs under
-// dK(j) and dP^T(j+1), and the dS phase of tile j under dV(j) and S^T(j+1).
+// TMEM: X [0, 128) fp32, taken by S^T and dP^T in turn | PT [128, 192) | DS [192, 256)
+// (bf16 pairs) | dV [256, 384) | dK [384, 512). The softmax warps read X out first
+// thing in each phase, so the next S^T or dP^T runs while they still work on this one;
+// P^T and dS^T wait in columns of their own for their dV / dK products. Two MMA issuers:
+// warp 9 the X products (S^T, dP^T, alternating), warp 10 the accumulating ones.
 constexpr int KV_STAGE_BYTES = 2 * TILE_BYTES + 3 * RT_BYTES;   // Q, dO, lo, lse2, delta
 constexpr int KV_STAGE_STRIDE = (KV_STAGE_BYTES + 1023) & ~1023;
 constexpr int KVB_SM_K = 0, KVB_SM_V = TILE_BYTES, KVB_SM_ST = 2 * TILE_BYTES;
 constexpr int KVB_SM_BAR = KVB_SM_ST + 2 * KV_STAGE_STRIDE;
-constexpr uint32_t KV_COL_A = 0, KV_COL_B = 128, KV_COL_DV = 256, KV_COL_DK = 384;
+constexpr uint32_t KV_COL_X = 0, KV_COL_PT = 128, KV_COL_DS = 192, KV_COL_DV = 256, KV_COL_DK = 384;
 
 struct KvbBars {
   uint64_t st_full[2], st_empty[2];
   uint64_t own_full, own_empty;
-  uint64_t s_full, dp_full, p_full, ds_full;
+  uint64_t s_full, dp_full, x_free;   // X products and their read-out
+  uint64_t p_full, ds_full;           // P^T / dS^T written
+  uint64_t pt_free, ds_free;          // dV / dK product done with PT / DS
   uint64_t acc_full, acc_empty;
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
@@ -264,13 +266,26 @@ __device__ __forceinline__ bool kv_producer(const CUtensorMap *tq, const CUtenso
   return ok;
 }
 
-__device__ __forceinline__ bool kv_mma(const BwArgs &a, uint8_t *smem, KvbBars *bars, uint32_t tmem, int lane) {
+// Issuer of the X products: S^T(j) = K Q_j^T then dP^T(j) = V dO_j^T, each once the
+// softmax warps have read the previous X product out (x_free). Releases K and V after
+// the item's last product.
+__device__ __forceinline__ bool kv_x_issuer(const BwArgs &a, uint8_t *smem, KvbBars *bars, uint32_t tmem, int lane) {
   volatile int *abort = &bars->abort;
   const uint32_t k_s = smem_u32(smem + KVB_SM_K), v_s = smem_u32(smem + KVB_SM_V);
   const uint32_t st0 = smem_u32(smem + KVB_SM_ST);
-  int use = 0, own = 0;
-  uint32_t pf_par = 0, dsf_par = 0, ae_par = 1;
+  int use = 0, own = 0, n_x = 0;
   bool ok = true;
+  auto x_product = [&](uint32_t a_s, uint32_t b_s, uint64_t *done) -> bool {
+    if (n_x > 0 && !mbar_wait(&bars->x_free, (n_x - 1) & 1, abort)) return false;
+    tc_fence_after();
+    if (lane == 0) {
+      mma_tile_kk(tmem + KV_COL_X, a_s, b_s, false);
+      mma_commit(done);
+    }
+    __syncwarp();
+    ++n_x;
+    return true;
+  };
   for (int it = 0; ok; ++it) {
     const int slot = it & 1;
     if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
@@ -282,25 +297,49 @@ __device__ __forceinline__ bool kv_mma(const BwArgs &a, uint8_t *smem, KvbBars *
     const int n = range_tiles(dkdv_range(a, I));
     if (!(ok = mbar_wait(&bars->own_full, it & 1, abort))) break;
     ++own;
-    tc_fence_after();
-    const int base = use;
-    auto q_s = [&](int j) { return st0 + uint32_t((base + j) & 1) * KV_STAGE_STRIDE; };
-    auto wait_stage = [&](int j) -> bool {
-      if (!mbar_wait(&bars->st_full[(base + j) & 1], ((base + j) >> 1) & 1, abort)) return false;
-      tc_fence_after();
-      return true;
-    };
-    if (n > 0) {
-      if (!(ok = wait_stage(0))) break;
-      if (lane == 0) {
-        mma_tile_kk(tmem + KV_COL_A, k_s, q_s(0), false);              // S^T(0) = K Q^T
-        mma_commit(&bars->s_full);
-        mma_tile_kk(tmem + KV_COL_B, v_s, q_s(0) + TILE_BYTES, false); // dP^T(0) = V dO^T
-        mma_commit(&bars->dp_full);
-      }
-      __syncwarp();
-    }
     for (int j = 0; j < n && ok; ++j) {
+      const int k = use + j;
+      if (!(ok = mbar_wait(&bars->st_full[k & 1], (k >> 1) & 1, abort))) break;
+      const uint32_t q_s = st0 + uint32_t(k & 1) * KV_STAGE_STRIDE;
+      if (!(ok = x_product(k_s, q_s, &bars->s_full))) break;               // S^T(j)
+      if (!(ok = x_product(v_s, q_s + TILE_BYTES, &bars->dp_full))) break;  // dP^T(j)
+    }
+    if (!ok) break;
+    use += n;
+    if (lane == 0) mma_commit(&bars->own_empty);
+    __syncwarp();
+  }
+  if (lane == 0) {
+    bars->use = use;
+    bars->own_used = own;
+  }
+  return ok;
+}
+
+// Issuer of the accumulating products: dV += P^T(j) dO_j once P^T is written, dK +=
+// dS^T(j) Q_j once dS^T is written; then releases the stage (its row terms were read
+// before dS^T was signalled). The first products of an item overwrite dV and dK once
+// the previous item's have been read out.
+__device__ __forceinline__ bool kv_acc_issuer(const BwArgs &a, uint8_t *smem, KvbBars *bars, uint32_t tmem,
+                                              int lane) {
+  volatile int *abort = &bars->abort;
+  const uint32_t st0 = smem_u32(smem + KVB_SM_ST);
+  int use = 0;
+  uint32_t pf_par = 0, dsf_par = 0, ae_par = 1;
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    const int slot = it & 1;
+    if (!(ok = mbar_wait(&bars->item_full[slot], (it >> 1) & 1, abort))) break;
+    const int item = bars->item[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+    if (item < 0) break;
+    const BwItem I = bw_decode(a, item);
+    const int n = range_tiles(dkdv_range(a, I));
+    for (int j = 0; j < n && ok; ++j) {
+      const int k = use + j;
+      if (!(ok = mbar_wait(&bars->st_full[k & 1], (k >> 1) & 1, abort))) break;
+      const uint32_t q_s = st0 + uint32_t(k & 1) * KV_STAGE_STRIDE;
       if (!(ok = mbar_wait(&bars->p_full, pf_par, abort))) break;
       pf_par ^= 1;
       if (j == 0) {
@@ -308,41 +347,25 @@ __device__ __forceinline__ bool kv_mma(const BwArgs &a, uint8_t *smem, KvbBars *
         ae_par ^= 1;
       }
       tc_fence_after();
-      if (lane == 0) mma_tile_ts(tmem + KV_COL_DV, tmem + KV_COL_A, q_s(j) + TILE_BYTES, j > 0);   // dV += P^T dO
-      __syncwarp();
-      const bool more = j + 1 < n;
-      if (more) {
-        if (!(ok = wait_stage(j + 1))) break;
-        if (lane == 0) {
-          mma_tile_kk(tmem + KV_COL_A, k_s, q_s(j + 1), false);   // S^T(j+1): A is free after dV(j) in order
-          mma_commit(&bars->s_full);
-        }
-        __syncwarp();
+      if (lane == 0) {
+        mma_tile_ts_packed(tmem + KV_COL_DV, tmem + KV_COL_PT, q_s + TILE_BYTES, j > 0);   // dV += P^T dO
+        mma_commit(&bars->pt_free);
       }
+      __syncwarp();
       if (!(ok = mbar_wait(&bars->ds_full, dsf_par, abort))) break;
       dsf_par ^= 1;
       tc_fence_after();
       if (lane == 0) {
-        mma_tile_ts(tmem + KV_COL_DK, tmem + KV_COL_B, q_s(j), j > 0);   // dK += dS^T Q
-        mma_commit(&bars->st_empty[(base + j) & 1]);
-        if (more) {
-          mma_tile_kk(tmem + KV_COL_B, v_s, q_s(j + 1) + TILE_BYTES, false);   // dP^T(j+1)
-          mma_commit(&bars->dp_full);
-        }
+        mma_tile_ts_packed(tmem + KV_COL_DK, tmem + KV_COL_DS, q_s, j > 0);   // dK += dS^T Q
+        mma_commit(&bars->ds_free);
+        mma_commit(&bars->st_empty[k & 1]);
       }
       __syncwarp();
     }
     if (!ok) break;
-    use = base + n;
-    if (lane == 0) {
-      if (n > 0) mma_commit(&bars->acc_full);
-      mma_commit(&bars->own_empty);
-    }
+    use += n;
+    if (lane == 0 && n > 0) mma_commit(&bars->acc_full);
     __syncwarp();
-  }
-  if (lane == 0) {
-    bars->use = use;
-    bars->own_used = own;
   }
   return ok;
 }
@@ -355,11 +378,12 @@ __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBa
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
   const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-  const uint32_t tA = tmem + lane_off + KV_COL_A + 64 * w;
-  const uint32_t tB = tmem + lane_off + KV_COL_B + 64 * w;
+  const uint32_t tX = tmem + lane_off + KV_COL_X + 64 * w;
+  const uint32_t tPT = tmem + lane_off + KV_COL_PT + 32 * w;
+  const uint32_t tDS = tmem + lane_off + KV_COL_DS + 32 * w;
   const float c = a.scale_log2;
   uint32_t sf_par = 0, dpf_par = 0, af_par = 0;
-  int use = 0;
+  int use = 0, n_done = 0;   // n_done: query tiles finished (all items), = dV / dK products issued before
   bool ok = true;
   for (int it = 0; ok; ++it) {
     const int slot = it & 1;
@@ -372,7 +396,7 @@ __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBa
     const TileRange R = dkdv_range(a, I);
     const int n = range_tiles(R);
     const int k0 = I.tile * BN, jk = k0 + row;   // this thread's key
-    for (int j = 0; j < n; ++j, ++use) {
+    for (int j = 0; j < n; ++j, ++use, ++n_done) {
       const int st = use & 1;
       const uint8_t *stage = smem + KVB_SM_ST + st * KV_STAGE_STRIDE;
       const int *lo_q = reinterpret_cast<const int *>(stage + 2 * TILE_BYTES);
@@ -386,6 +410,18 @@ __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBa
       // the stage's row terms arrived by bulk copy: observe the stage's barrier
       if (!(ok = mbar_wait(&bars->st_full[st], (use >> 1) & 1, abort))) break;
       tc_fence_after();
+      float p[64];
+      {
+        uint32_t sv[64];
+        tmem_ld32(tX, sv);
+        tmem_ld32(tX + 32, sv + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->x_free);   // S^T is in registers: X may take dP^T
+#pragma unroll
+        for (int e = 0; e < 64; ++e) p[e] = __uint_as_float(sv[e]);
+      }
       // Key jk is visible from query q0 + q iff lo[q0 + q] <= jk <= q0 + q; lo is
       // non-decreasing, so these q form one range [q_from, q_to).
       const bool full = lo_q[BM - 1] <= k0 && k0 + BN - 1 <= q0;
@@ -401,30 +437,29 @@ __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBa
       }
       q_from -= 64 * w;
       q_to -= 64 * w;
-      float p[64];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t sv[16];
-        tmem_ld16(tA + ch * 16, sv);
-        tmem_ld_wait();
+      for (int e4 = 0; e4 < 16; ++e4) {
+        const float4 l2 = l2_q[e4];
+        const float l2v[4] = {l2.x, l2.y, l2.z, l2.w};
 #pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
-          const float4 l2 = l2_q[ch * 4 + e4];
-          const float l2v[4] = {l2.x, l2.y, l2.z, l2.w};
+        for (int e = 0; e < 4; ++e) p[e4 * 4 + e] = ex2_approx(fmaf(p[e4 * 4 + e], c, -l2v[e]));
+      }
+      if (!full) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) p[ch * 16 + e4 * 4 + e] = ex2_approx(fmaf(__uint_as_float(sv[e4 * 4 + e]), c, -l2v[e]));
+        for (int q = 0; q < 64; ++q)
+          if (q < q_from || q >= q_to) p[q] = 0.f;
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+        // PT belongs to the previous dV product until it completes
+        if (n_done > 0) {
+          if (!(ok = mbar_wait(&bars->pt_free, (n_done - 1) & 1, abort))) break;
+          tc_fence_after();
         }
-        if (!full) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int q = ch * 16 + e;
-            if (q < q_from || q >= q_to) p[q] = 0.f;
-          }
-        }
-        uint32_t pk[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(p[ch * 16 + 2 * e], p[ch * 16 + 2 * e + 1]);
-        tmem_st8(tA + ch * 16, pk);
+        tmem_st16(tPT, pk);
+        tmem_st16(tPT + 16, pk + 16);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -435,26 +470,35 @@ __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBa
       if (!(ok = mbar_wait(&bars->dp_full, dpf_par, abort))) break;
       dpf_par ^= 1;
       tc_fence_after();
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t dv[16];
-        tmem_ld16(tB + ch * 16, dv);
+      uint32_t dk[32];
+      {
+        uint32_t dv[64];
+        tmem_ld32(tX, dv);
+        tmem_ld32(tX + 32, dv + 32);
         tmem_ld_wait();
-        uint32_t dk[8];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->x_free);   // dP^T is in registers: X may take S^T(j+1)
 #pragma unroll
-        for (int e4 = 0; e4 < 4; e4 += 2) {
-          const float4 d0 = dl_q[ch * 4 + e4], d1 = dl_q[ch * 4 + e4 + 1];
+        for (int e4 = 0; e4 < 16; e4 += 2) {
+          const float4 d0 = dl_q[e4], d1 = dl_q[e4 + 1];
           const float dlv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
-            const int q = ch * 16 + e4 * 4 + e;
-            const float s0 = p[q] * (__uint_as_float(dv[e4 * 4 + e]) - dlv[e]);
-            const float s1 = p[q + 1] * (__uint_as_float(dv[e4 * 4 + e + 1]) - dlv[e + 1]);
-            dk[(e4 * 4 + e) / 2] = pack_bf16x2(s0, s1);
+            const int q = e4 * 4 + e;
+            const float s0 = p[q] * (__uint_as_float(dv[q]) - dlv[e]);
+            const float s1 = p[q + 1] * (__uint_as_float(dv[q + 1]) - dlv[e + 1]);
+            dk[q / 2] = pack_bf16x2(s0, s1);
           }
         }
-        tmem_st8(tB + ch * 16, dk);
       }
+      // DS belongs to the previous dK product until it completes
+      if (n_done > 0) {
+        if (!(ok = mbar_wait(&bars->ds_free, (n_done - 1) & 1, abort))) break;
+        tc_fence_after();
+      }
+      tmem_st16(tDS, dk);
+      tmem_st16(tDS + 16, dk + 16);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -495,17 +539,20 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       mbar_init(&bars->st_full[s], 1);
       mbar_init(&bars->st_empty[s], 1);
       mbar_init(&bars->item_full[s], 1);
-      mbar_init(&bars->item_empty[s], 9);   // softmax 8 + MMA 1 warps
+      mbar_init(&bars->item_empty[s], 10);   // softmax 8 + MMA 2 warps
     }
     mbar_init(&bars->own_full, 1);
     mbar_init(&bars->own_empty, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->x_free, 8);
     mbar_init(&bars->p_full, 8);
     mbar_init(&bars->ds_full, 8);
+    mbar_init(&bars->pt_free, 1);
+    mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 2);
     bars->abort = 0;
     bars->fill = bars->use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
@@ -531,7 +578,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     if (lane == 0) ok = kv_producer(&tq, &tk, &tv, &tdo, a, smem, bars);
     __syncwarp();
   } else if (warp == BW_MMA) {
-    ok = kv_mma(a, smem, bars, tmem, lane);
+    ok = kv_x_issuer(a, smem, bars, tmem, lane);
+  } else if (warp == BW_MMA2) {
+    ok = kv_acc_issuer(a, smem, bars, tmem, lane);
   }
 
   if (!ok) {
@@ -545,7 +594,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       for (int k = bars->use; k < bars->fill; ++k) bounded_wait_plain_bw(&bars->st_full[k & 1], (k >> 1) & 1);
       if (bars->own_issued > bars->own_used) bounded_wait_plain_bw(&bars->own_full, (bars->own_issued - 1) & 1);
     }
-    if (warp == BW_MMA && lane == 0) {
+    if ((warp == BW_MMA || warp == BW_MMA2) && lane == 0) {
       mma_commit(&bars->drain);
       bounded_wait_plain_bw(&bars->drain, 0);
     }

@@ -339,6 +339,14 @@ __device__ __forceinline__ void mma_tile_ts(uint32_t d_tmem, uint32_t x_tmem, ui
            IDESC_128_KM, (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// The same product with X packed contiguously in TMEM: inner block kk at x_tmem + 8 kk.
+__device__ __forceinline__ void mma_tile_ts_packed(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_s, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts(d_tmem, x_tmem + uint32_t(kk) * 8, sdesc_sw128(y_s + uint32_t(kk) * 2048, HALF_BYTES, 1024),
+           IDESC_128_KM, (accumulate || kk > 0) ? 1u : 0u);
+}
+
 // ----------------------------------------------------------------------------- tile ranges
 // Inclusive range of key tiles that query tile [q0, q0+BM) of one batch row needs.
 // `lo_row[i]` is the first key visible to query i (its document start; i+1 for
