@@ -15,8 +15,7 @@
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer (and the scheduler ticket)
 //   warp  9    tcgen05 issuer of the S = Q K^T products (and TMEM owner)
-//   warp  10   tcgen05 issuer of the O += P V products
-//   warp  11   idle (it keeps 3 warps per SM sub-partition)
+//   warps 10, 11  tcgen05 issuers of the O_t += P_t V products of query tile 0, 1
 // TMEM (512 columns): S (128 fp32 columns, shared by the two query tiles in turn) |
 // P0 | P1 (64 columns each, bf16 pairs) | O0 | O1 (128 fp32 columns each). Because P
 // has columns of its own, the S product of the next key tile does not wait for the P.V
@@ -33,8 +32,10 @@ constexpr int FWD_WARPS = 12;   // 3 warps per SM sub-partition: 168 registers e
 constexpr int FWD_THREADS = FWD_WARPS * 32;
 constexpr int WARP_PRODUCER = 8;
 constexpr int WARP_MMA = 9;    // issuer of the S products (and TMEM owner)
-constexpr int WARP_MMA2 = 10;  // issuer of the P.V products
+constexpr int WARP_PV0 = 10;   // issuers of the P.V products of query tiles 0 and 1
+constexpr int WARP_PV1 = 11;
 constexpr int KV_STAGES = 4;
+static_assert(KV_STAGES % 2 == 0, "K tiles take the even stages, V tiles the odd ones");
 
 constexpr int SM_Q = 0;
 constexpr int SM_KV = 2 * TILE_BYTES;
@@ -49,7 +50,8 @@ struct FwdBars {
   int item[2];
   uint32_t tmem_base;
   int abort;
-  int kv_fill, kv_use_k, kv_use_v, q_issued, q_used;
+  int kv_fill, kv_use_k, kv_use_v[2], q_issued, q_used;
+  int s_issued[2];   // S products of query tile t issued so far
 };
 
 constexpr int FWD_SMEM = SM_BAR + int(sizeof(FwdBars)) + 1024;   // + alignment slack
@@ -182,7 +184,7 @@ __device__ bool s_issuer_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, ui
                               int lane) {
   volatile int *abort = &bars->abort;
   const uint32_t kv_s0 = smem_u32(smem + SM_KV);
-  int kv_use = 0, q_used = 0, n_s = 0;
+  int kv_use = 0, q_used = 0, n_s = 0, n_st[2] = {0, 0};
   bool ok = true;
   for (int it = 0;; ++it) {
     const int slot = it & 1;
@@ -210,6 +212,7 @@ __device__ bool s_issuer_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, ui
         if (lane == 0) {
           issue_qk(tmem + COL_S, smem_u32(smem + SM_Q + t * TILE_BYTES), kv_s0 + stK * TILE_BYTES);
           mma_commit(&bars->s_full[t]);
+          reinterpret_cast<volatile int *>(bars->s_issued)[t] = ++n_st[t];
         }
         __syncwarp();
         ++n_s;
@@ -233,15 +236,32 @@ __device__ bool s_issuer_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, ui
   return ok;
 }
 
-// P.V issuer: per key tile in ring order, O_0 += P_0 V then O_1 += P_1 V (each once its
-// softmax has written P_t and rescaled O_t), then releases the V stage. The first
+// Spins (bounded, like mbar_wait) until *count reaches target.
+__device__ __forceinline__ bool wait_count(volatile int *count, int target, volatile int *abort) {
+  if (*count >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1; *count < target; ++it) {
+    if ((it & 63u) == 0u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    }
+  }
+  return true;
+}
+
+// P.V issuer of query tile t: per key tile in ring order, O_t += P_t V once the softmax
+// has written P_t and rescaled O_t, then its share of the V stage's release. The first
 // product of an item overwrites O_t once the previous item's O_t has been read out.
+// P_t V of key tile j enters the tensor core's queue after S_t of key tile j + 1 (when
+// the tile sees it): the softmax waits for that S, not for the P.V product. One issuer
+// per tile, so that neither tile's P.V waits for the other's S.
 __device__ bool pv_issuer_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_t tmem, int kv_chunk,
-                               int lane) {
+                               int t, int lane) {
   volatile int *abort = &bars->abort;
+  volatile int *s_issued = bars->s_issued + t;
   const uint32_t kv_s0 = smem_u32(smem + SM_KV);
-  int kv_use = 0;
-  uint32_t pf_par[2] = {0, 0}, oe_par[2] = {1, 1};
+  int kv_use = 0, n_pv = 0;
+  uint32_t pf_par = 0, oe_par = 1;
   bool ok = true;
   for (int it = 0;; ++it) {
     const int slot = it & 1;
@@ -252,41 +272,40 @@ __device__ bool pv_issuer_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, u
     if (item < 0) break;
     const Item I = decode(a, item);
     const Ranges R = item_ranges(a, I);
-    bool first[2] = {true, true};
+    const TileRange my = R.r[t];
+    bool first = true;
     KvSeq seq;
     for (seq.init(R.first, R.last, kv_chunk); seq.valid() && ok; seq.next()) {
       const int stV = (kv_use + 1) % KV_STAGES, parV = ((kv_use + 1) / KV_STAGES) & 1;
       if (!(ok = mbar_wait(&bars->kv_full[stV], parV, abort))) break;
       kv_use += 2;
-      bool used = false;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (!R.r[t].has(seq.t)) continue;
-        if (first[t]) {
-          if (!(ok = mbar_wait(&bars->o_empty[t], oe_par[t], abort))) break;
-          oe_par[t] ^= 1;
-        }
-        if (!(ok = mbar_wait(&bars->p_full[t], pf_par[t], abort))) break;
-        pf_par[t] ^= 1;
-        tc_fence_after();
-        if (lane == 0) {
-          issue_pv(tmem + col_o(t), tmem + col_p(t), kv_s0 + stV * TILE_BYTES, !first[t]);
-          mma_commit(&bars->pv_done[t]);
-        }
+      if (!my.has(seq.t)) {
+        if (lane == 0) mbar_arrive(&bars->kv_empty[stV]);
         __syncwarp();
-        first[t] = false;
-        used = true;
+        continue;
       }
-      if (!ok) break;
+      if (first) {
+        if (!(ok = mbar_wait(&bars->o_empty[t], oe_par, abort))) break;
+        oe_par ^= 1;
+      }
+      if (!(ok = mbar_wait(&bars->p_full[t], pf_par, abort))) break;
+      pf_par ^= 1;
+      KvSeq nx = seq;
+      nx.next();
+      if (nx.valid() && my.has(nx.t) && !(ok = wait_count(s_issued, n_pv + 2, abort))) break;
+      ++n_pv;
+      tc_fence_after();
       if (lane == 0) {
-        if (used) mma_commit(&bars->kv_empty[stV]);
-        else mbar_arrive(&bars->kv_empty[stV]);
+        issue_pv(tmem + col_o(t), tmem + col_p(t), kv_s0 + stV * TILE_BYTES, !first);
+        mma_commit(&bars->pv_done[t]);
+        mma_commit(&bars->kv_empty[stV]);
       }
       __syncwarp();
+      first = false;
     }
     if (!ok) break;
   }
-  if (lane == 0) bars->kv_use_v = kv_use;
+  if (lane == 0) bars->kv_use_v[t] = kv_use;
   return ok;
 }
 
@@ -472,7 +491,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < KV_STAGES; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);   // K stages: the S issuer; V stages: the P.V issuer
+      mbar_init(&bars->kv_empty[s], (s & 1) ? 2 : 1);   // K stages: the S issuer; V stages: both P.V issuers
     }
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
@@ -483,11 +502,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       mbar_init(&bars->pv_done[t], 1);
       mbar_init(&bars->o_empty[t], 4);
       mbar_init(&bars->item_full[t], 1);
-      mbar_init(&bars->item_empty[t], 10);   // softmax 8 + MMA 2 warps
+      mbar_init(&bars->item_empty[t], 11);   // softmax 8 + MMA 3 warps
     }
-    mbar_init(&bars->drain, 2);
+    mbar_init(&bars->drain, 3);
     bars->abort = 0;
-    bars->kv_fill = bars->kv_use_k = bars->kv_use_v = bars->q_issued = bars->q_used = 0;
+    bars->kv_fill = bars->kv_use_k = bars->kv_use_v[0] = bars->kv_use_v[1] = bars->q_issued = bars->q_used = 0;
+    bars->s_issued[0] = bars->s_issued[1] = 0;
     fence_mbar_init();
   }
   if (warp == WARP_MMA) {
@@ -510,8 +530,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     __syncwarp();
   } else if (warp == WARP_MMA) {
     ok = s_issuer_role(a, smem, bars, tmem, kv_chunk, lane);
-  } else if (warp == WARP_MMA2) {
-    ok = pv_issuer_role(a, smem, bars, tmem, kv_chunk, lane);
+  } else if (warp == WARP_PV0 || warp == WARP_PV1) {
+    ok = pv_issuer_role(a, smem, bars, tmem, kv_chunk, warp - WARP_PV0, lane);
   } else if (warp < 8) {
     ok = softmax_role(a, bars, tmem, kv_chunk, warp >> 2, warp, lane);
   }
@@ -525,13 +545,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     // Let copies and MMAs still in flight land before shared memory and TMEM go away.
     if (warp == WARP_PRODUCER && lane == 0) {
       // loads no consumer has waited for: K (even n) from the S issuer's count, V (odd n)
-      // from the P.V issuer's
-      for (int n = min(bars->kv_use_k, bars->kv_use_v); n < bars->kv_fill; ++n)
-        if (n >= ((n & 1) ? bars->kv_use_v : bars->kv_use_k))
+      // from the further of the P.V issuers' counts
+      const int use_v = max(bars->kv_use_v[0], bars->kv_use_v[1]);
+      for (int n = min(bars->kv_use_k, use_v); n < bars->kv_fill; ++n)
+        if (n >= ((n & 1) ? use_v : bars->kv_use_k))
           bounded_wait_plain(&bars->kv_full[n % KV_STAGES], (n / KV_STAGES) & 1);
       if (bars->q_issued > bars->q_used) bounded_wait_plain(&bars->q_full, (bars->q_issued - 1) & 1);
     }
-    if ((warp == WARP_MMA || warp == WARP_MMA2) && lane == 0) {
+    if ((warp == WARP_MMA || warp == WARP_PV0 || warp == WARP_PV1) && lane == 0) {
       mma_commit(&bars->drain);
       bounded_wait_plain(&bars->drain, 0);
     }
