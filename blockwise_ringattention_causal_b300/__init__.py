@@ -22,7 +22,7 @@ __all__ = [
     "LwmError", "library_path", "load_library",
     "lwm_attn_workspace_size", "lwm_attn_workspace_size_fwd", "lwm_attn_prepare", "lwm_attn_fwd", "lwm_attn_fwd_ring",
     "lwm_attn_fwd_prepared", "lwm_attn_bwd", "lwm_attn_bwd_prepared", "lwm_attn_bwd_stages",
-    "lwm_attn_check",
+    "lwm_attn_check", "lwm_attn_set_wait_limit",
     "lwm_status_string", "lwm_last_error", "new_workspace", "forward", "backward",
 ]
 
@@ -50,6 +50,7 @@ _SIGNATURES = {
     "lwm_status_string": (ctypes.c_char_p, [_I]),
     "lwm_last_error": (ctypes.c_char_p, []),
     "lwm_attn_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "lwm_attn_set_wait_limit": (_I, [_P, ctypes.c_uint64, _P]),
 }
 
 
@@ -230,6 +231,12 @@ def lwm_attn_bwd_stages(q, k, v, out, dout, lse, dq, dk, dv, stages, workspace, 
                                               _ptr(dq), _ptr(dk), _ptr(dv), B, S, H, D, int(stages),
                                               _ptr(workspace), workspace.numel(), _stream(stream)),
            "lwm_attn_bwd_stages")
+
+
+def lwm_attn_set_wait_limit(workspace, limit_ns, stream=None):
+    """Bound of the kernels' pipeline waits for calls with this workspace (0 = default 2 s)."""
+    _check(load_library().lwm_attn_set_wait_limit(_ptr(workspace), int(limit_ns), _stream(stream)),
+           "lwm_attn_set_wait_limit")
 
 
 def lwm_attn_check(workspace, stream=None) -> int:

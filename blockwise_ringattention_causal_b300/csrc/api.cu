@@ -113,6 +113,8 @@ bool make_dqacc_map(CUtensorMap *m, void *ws, int B, int S, int H) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
+}  // namespace
+
 lwm_status check_sizes(int B, int S, int H, int D) {
   if (B <= 0 || S <= 0 || H <= 0 || D <= 0) return LWM_ERR_INVALID_ARG;
   if (D != HD) return LWM_ERR_UNSUPPORTED;
@@ -122,6 +124,13 @@ lwm_status check_sizes(int B, int S, int H, int D) {
   if (static_cast<long long>(B) * nT * H >= (1ll << 31)) return LWM_ERR_INVALID_ARG;
   return LWM_OK;
 }
+
+lwm_status check_device() {
+  DeviceInfo d;
+  return device_info(d);
+}
+
+namespace {
 
 // `with_dqacc`: the call runs the single-kernel backward pass, which needs the whole
 // layout; every other call needs only the part in front of the dQ accumulator.
@@ -157,6 +166,8 @@ lwm_status fwd_common(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, l
   Problem p{B, S, H, d.num_sms};
   return from_cuda(launch_fwd(tq, tk, tv, out, lse, p, ws, stream));
 }
+
+__global__ void set_u64_kernel(unsigned long long *p, unsigned long long v) { *p = v; }
 
 lwm_status check_fwd_args(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, lwm_bf16 *out, float *lse,
                           int B, int S, int H, int D, void *ws, size_t ws_bytes) {
@@ -346,6 +357,14 @@ lwm_status lwm_attn_check(void *workspace, lwm_stream stream) {
   if (word & ERRBIT_SEGMENTS) return LWM_ERR_SEGMENTS;
   if (word & ERRBIT_TIMEOUT) return LWM_ERR_TIMEOUT;
   return LWM_OK;
+}
+
+lwm_status lwm_attn_set_wait_limit(void *workspace, uint64_t limit_ns, lwm_stream stream) {
+  if (!workspace) return LWM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LWM_ERR_WORKSPACE;
+  auto *word = reinterpret_cast<unsigned long long *>(static_cast<int *>(workspace) + HDR_WAIT_LIMIT);
+  set_u64_kernel<<<1, 1, 0, stream>>>(word, static_cast<unsigned long long>(limit_ns));
+  return from_cuda(cudaGetLastError());
 }
 
 const char *lwm_last_error(void) { return g_last_error; }

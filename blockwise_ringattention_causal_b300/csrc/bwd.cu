@@ -117,13 +117,6 @@ __device__ __forceinline__ void load_tile(const CUtensorMap *m, uint64_t *bar, u
   tma_load_4d(m, bar, dst + HALF_BYTES, 64, h, row0, b);
 }
 
-__device__ bool bounded_wait_plain_bw(uint64_t *bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
-  return true;
-}
-
 // Writes 64 fp32 TMEM columns of this thread's lane, scaled by f, as bf16 to dst.
 __device__ __forceinline__ void store_cols_bf16(uint32_t t_addr, float f, __nv_bfloat16 *dst, bool valid) {
 #pragma unroll 1
@@ -218,7 +211,7 @@ struct KvbBars {
   uint64_t drain;
   int item[2];
   uint32_t tmem_base;
-  int abort;
+  WaitCtl ctl;
   int fill, use, own_issued, own_used;
 };
 constexpr int KVB_SMEM = KVB_SM_BAR + int(sizeof(KvbBars)) + 1024;
@@ -226,7 +219,7 @@ static_assert(KVB_SMEM <= 232448, "shared memory budget of one CTA");
 
 __device__ __forceinline__ bool kv_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                                             const CUtensorMap *tdo, const BwArgs &a, uint8_t *smem, KvbBars *bars) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   int fill = 0, own = 0;
   bool ok = true;
   for (int it = 0;; ++it) {
@@ -270,10 +263,11 @@ __device__ __forceinline__ bool kv_producer(const CUtensorMap *tq, const CUtenso
 // softmax warps have read the previous X product out (x_free). Releases K and V after
 // the item's last product.
 __device__ __forceinline__ bool kv_x_issuer(const BwArgs &a, uint8_t *smem, KvbBars *bars, uint32_t tmem, int lane) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   const uint32_t k_s = smem_u32(smem + KVB_SM_K), v_s = smem_u32(smem + KVB_SM_V);
   const uint32_t st0 = smem_u32(smem + KVB_SM_ST);
   int use = 0, own = 0, n_x = 0;
+  int seen = 0;   // stages whose arrival this warp has observed (the abort path waits for the rest)
   bool ok = true;
   auto x_product = [&](uint32_t a_s, uint32_t b_s, uint64_t *done) -> bool {
     if (n_x > 0 && !mbar_wait(&bars->x_free, (n_x - 1) & 1, abort)) return false;
@@ -300,6 +294,7 @@ __device__ __forceinline__ bool kv_x_issuer(const BwArgs &a, uint8_t *smem, KvbB
     for (int j = 0; j < n && ok; ++j) {
       const int k = use + j;
       if (!(ok = mbar_wait(&bars->st_full[k & 1], (k >> 1) & 1, abort))) break;
+      seen = k + 1;
       const uint32_t q_s = st0 + uint32_t(k & 1) * KV_STAGE_STRIDE;
       if (!(ok = x_product(k_s, q_s, &bars->s_full))) break;               // S^T(j)
       if (!(ok = x_product(v_s, q_s + TILE_BYTES, &bars->dp_full))) break;  // dP^T(j)
@@ -310,7 +305,7 @@ __device__ __forceinline__ bool kv_x_issuer(const BwArgs &a, uint8_t *smem, KvbB
     __syncwarp();
   }
   if (lane == 0) {
-    bars->use = use;
+    bars->use = seen;
     bars->own_used = own;
   }
   return ok;
@@ -322,7 +317,7 @@ __device__ __forceinline__ bool kv_x_issuer(const BwArgs &a, uint8_t *smem, KvbB
 // the previous item's have been read out.
 __device__ __forceinline__ bool kv_acc_issuer(const BwArgs &a, uint8_t *smem, KvbBars *bars, uint32_t tmem,
                                               int lane) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   const uint32_t st0 = smem_u32(smem + KVB_SM_ST);
   int use = 0;
   uint32_t pf_par = 0, dsf_par = 0, ae_par = 1;
@@ -374,7 +369,7 @@ __device__ __forceinline__ bool kv_acc_issuer(const BwArgs &a, uint8_t *smem, Kv
 // [64 w, 64 w + 64) of every streamed tile.
 __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBars *bars, uint32_t tmem, int w,
                                            int warp, int lane) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
   const uint32_t lane_off = uint32_t(quarter * 32) << 16;
@@ -553,7 +548,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 2);
-    bars->abort = 0;
+    bars->ctl.abort = 0;
+    bars->ctl.limit_ns = pipeline_wait_limit(a.hdr);
     bars->fill = bars->use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
   }
@@ -584,19 +580,19 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   }
 
   if (!ok) {
-    bars->abort = 1;
+    bars->ctl.abort = 1;
     raise_error(a.hdr + HDR_ERR, ERRBIT_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
-  if (bars->abort) {
+  if (bars->ctl.abort) {
     if (warp == BW_PRODUCER && lane == 0) {
-      for (int k = bars->use; k < bars->fill; ++k) bounded_wait_plain_bw(&bars->st_full[k & 1], (k >> 1) & 1);
-      if (bars->own_issued > bars->own_used) bounded_wait_plain_bw(&bars->own_full, (bars->own_issued - 1) & 1);
+      for (int k = bars->use; k < bars->fill; ++k) bounded_wait_plain(&bars->st_full[k & 1], (k >> 1) & 1);
+      if (bars->own_issued > bars->own_used) bounded_wait_plain(&bars->own_full, (bars->own_issued - 1) & 1);
     }
     if ((warp == BW_MMA || warp == BW_MMA2) && lane == 0) {
       mma_commit(&bars->drain);
-      bounded_wait_plain_bw(&bars->drain, 0);
+      bounded_wait_plain(&bars->drain, 0);
     }
     __syncthreads();
   }
@@ -633,13 +629,17 @@ constexpr uint32_t DQ_COL_B = 256, DQ_COL_C = 384;
 struct DqBars {
   uint64_t k_full[DQ_KSTAGES], k_empty[DQ_KSTAGES], v_full[DQ_VSTAGES], v_empty[DQ_VSTAGES];
   uint64_t own_full, own_empty;
-  uint64_t s_full[2], dp_full, ds_full;
+  // dS(j) written: ds_full[j % 2] is waited by chain 0 (slot A_{j % 2}), ds_dp by chain 1.
+  // One barrier per slot: chain 0 issues S(j + 2) only after its wait for dS(j), so the
+  // softmax cannot complete a second phase of that slot's barrier before the wait (a
+  // single barrier could run two phases ahead and alias the parity).
+  uint64_t s_full[2], dp_full, ds_full[2], ds_dp;
   uint64_t acc_full, acc_empty;
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   int item[2];
   uint32_t tmem_base;
-  int abort;
+  WaitCtl ctl;
   int k_fill, k_use, v_fill, v_use, own_issued, own_used;
 };
 constexpr int DQ_SMEM = DQ_SM_BAR + int(sizeof(DqBars)) + 1024;
@@ -647,7 +647,7 @@ static_assert(DQ_SMEM <= 232448, "shared memory budget of one CTA");
 
 __device__ __forceinline__ bool dq_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                                             const CUtensorMap *tdo, const BwArgs &a, uint8_t *smem, DqBars *bars) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   int k_fill = 0, v_fill = 0, own = 0;
   bool ok = true;
   for (int it = 0;; ++it) {
@@ -693,11 +693,12 @@ __device__ __forceinline__ bool dq_producer(const CUtensorMap *tq, const CUtenso
 // dO V_j^T into B, each after the softmax has finished reading the previous dP.
 __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *bars, uint32_t tmem, int chain,
                                        int lane) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   const uint32_t q_s = smem_u32(smem + DQ_SM_Q), do_s = smem_u32(smem + DQ_SM_DO);
   const uint32_t k0_s = smem_u32(smem + DQ_SM_K), v0_s = smem_u32(smem + DQ_SM_V);
   int k_use = 0, v_use = 0, own = 0, dp_issued = 0;
-  uint32_t dsf_par = 0, ae_par = 1;
+  int k_seen = 0;   // K stages whose arrival chain 0 has observed (the abort path waits for the rest)
+  uint32_t dsf_par[2] = {0, 0}, dsp_par = 0, ae_par = 1;
   bool ok = true;
   for (int it = 0; ok; ++it) {
     const int slot = it & 1;
@@ -716,6 +717,7 @@ __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *b
       auto k_s = [&](int j) { return k0_s + uint32_t((kb + j) % DQ_KSTAGES) * TILE_BYTES; };
       auto issue_s = [&](int j) -> bool {   // S(j) = Q K_j^T into A_{j % 2}
         if (!mbar_wait(&bars->k_full[(kb + j) % DQ_KSTAGES], ((kb + j) / DQ_KSTAGES) & 1, abort)) return false;
+        k_seen = kb + j + 1;
         tc_fence_after();
         if (lane == 0) {
           mma_tile_kk(tmem + uint32_t(j & 1) * 128, q_s, k_s(j), false);
@@ -726,8 +728,8 @@ __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *b
       };
       if (n > 0) ok = issue_s(0) && (n < 2 || issue_s(1));
       for (int j = 0; j < n && ok; ++j) {
-        if (!(ok = mbar_wait(&bars->ds_full, dsf_par, abort))) break;
-        dsf_par ^= 1;
+        if (!(ok = mbar_wait(&bars->ds_full[j & 1], dsf_par[j & 1], abort))) break;
+        dsf_par[j & 1] ^= 1;
         if (j == 0) {
           if (!(ok = mbar_wait(&bars->acc_empty, ae_par, abort))) break;
           ae_par ^= 1;
@@ -748,8 +750,8 @@ __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *b
         const int vs = v_use % DQ_VSTAGES;
         if (!(ok = mbar_wait(&bars->v_full[vs], (v_use / DQ_VSTAGES) & 1, abort))) break;
         if (dp_issued > 0) {   // B still holds the previous dP until its dS phase is done
-          if (!(ok = mbar_wait(&bars->ds_full, dsf_par, abort))) break;
-          dsf_par ^= 1;
+          if (!(ok = mbar_wait(&bars->ds_dp, dsp_par, abort))) break;
+          dsp_par ^= 1;
         }
         tc_fence_after();
         if (lane == 0) {
@@ -766,7 +768,7 @@ __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *b
     __syncwarp();
   }
   if (lane == 0 && chain == 0) {
-    bars->k_use = k_use;
+    bars->k_use = k_seen;
     bars->own_used = own;
   }
   if (lane == 0 && chain == 1) bars->v_use = v_use;
@@ -776,7 +778,7 @@ __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *b
 // Softmax warpgroup w of the dQ kernel: thread = query row `row`; key columns
 // [64 w, 64 w + 64) of every streamed tile.
 __device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32_t tmem, int w, int warp, int lane) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
   const uint32_t lane_off = uint32_t(quarter * 32) << 16;
@@ -861,7 +863,10 @@ __device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->ds_full);
+      if (lane == 0) {
+        mbar_arrive(&bars->ds_full[j & 1]);
+        mbar_arrive(&bars->ds_dp);
+      }
     }
     if (!ok) break;
 
@@ -900,17 +905,19 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->ds_full[s], 8);
       mbar_init(&bars->item_full[s], 1);
       mbar_init(&bars->item_empty[s], 10);  // softmax 8 + MMA 2 warps
     }
     mbar_init(&bars->own_full, 1);
     mbar_init(&bars->own_empty, 2);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->ds_full, 8);
+    mbar_init(&bars->ds_dp, 8);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 2);
-    bars->abort = 0;
+    bars->ctl.abort = 0;
+    bars->ctl.limit_ns = pipeline_wait_limit(a.hdr);
     bars->k_fill = bars->k_use = bars->v_fill = bars->v_use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
   }
@@ -939,22 +946,22 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   }
 
   if (!ok) {
-    bars->abort = 1;
+    bars->ctl.abort = 1;
     raise_error(a.hdr + HDR_ERR, ERRBIT_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
-  if (bars->abort) {
+  if (bars->ctl.abort) {
     if (warp == BW_PRODUCER && lane == 0) {
       for (int k = bars->k_use; k < bars->k_fill; ++k)
-        bounded_wait_plain_bw(&bars->k_full[k % DQ_KSTAGES], (k / DQ_KSTAGES) & 1);
+        bounded_wait_plain(&bars->k_full[k % DQ_KSTAGES], (k / DQ_KSTAGES) & 1);
       for (int k = bars->v_use; k < bars->v_fill; ++k)
-        bounded_wait_plain_bw(&bars->v_full[k % DQ_VSTAGES], (k / DQ_VSTAGES) & 1);
-      if (bars->own_issued > bars->own_used) bounded_wait_plain_bw(&bars->own_full, (bars->own_issued - 1) & 1);
+        bounded_wait_plain(&bars->v_full[k % DQ_VSTAGES], (k / DQ_VSTAGES) & 1);
+      if (bars->own_issued > bars->own_used) bounded_wait_plain(&bars->own_full, (bars->own_issued - 1) & 1);
     }
     if ((warp == BW_MMA || warp == BW_MMA2) && lane == 0) {
       mma_commit(&bars->drain);
-      bounded_wait_plain_bw(&bars->drain, 0);
+      bounded_wait_plain(&bars->drain, 0);
     }
     __syncthreads();
   }
@@ -999,11 +1006,10 @@ BwArgs bw_args(const Problem &p, void *workspace, const int *list) {
 
 cudaError_t launch_dkdv(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                         void *dk, void *dv, const Problem &p, void *workspace, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KVB_SMEM);
+  static std::atomic<uint64_t> attr_done{0};
+  {
+    const cudaError_t e = smem_attr_once(reinterpret_cast<const void *>(dkdv_kernel), KVB_SMEM, attr_done);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const Workspace w = Workspace::layout(p.B, p.S, p.H);
   BwArgs a = bw_args(p, workspace, reinterpret_cast<const int *>(static_cast<char *>(workspace) + w.off_list_kv));
@@ -1016,11 +1022,10 @@ cudaError_t launch_dkdv(const CUtensorMap &tq, const CUtensorMap &tk, const CUte
 
 cudaError_t launch_dq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                       void *dq, const Problem &p, void *workspace, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
+  static std::atomic<uint64_t> attr_done{0};
+  {
+    const cudaError_t e = smem_attr_once(reinterpret_cast<const void *>(dq_kernel), DQ_SMEM, attr_done);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const Workspace w = Workspace::layout(p.B, p.S, p.H);
   BwArgs a = bw_args(p, workspace, reinterpret_cast<const int *>(static_cast<char *>(workspace) + w.off_list_q));

@@ -74,7 +74,7 @@ struct FbBars {
   uint64_t drain;
   int item[2];
   uint32_t tmem_base;
-  int abort;
+  WaitCtl ctl;
   int q_fill, q_use, do_fill, do_use, own_issued, own_used;
 };
 constexpr int FB_SMEM = FB_SM_BAR + int(sizeof(FbBars)) + 1024;
@@ -168,13 +168,6 @@ __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk
 // Waits until every committed bulk group has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-__device__ bool fb_wait_plain(uint64_t *bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
-  return true;
-}
-
 __device__ __forceinline__ void fb_load_tile(const CUtensorMap *m, uint64_t *bar, uint8_t *dst, int h, int row0,
                                              int b) {
   tma_load_4d(m, bar, dst, 0, h, row0, b);
@@ -184,7 +177,7 @@ __device__ __forceinline__ void fb_load_tile(const CUtensorMap *m, uint64_t *bar
 // ----------------------------------------------------------------------------- producer
 __device__ __forceinline__ bool fb_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                                             const CUtensorMap *tdo, const FbArgs &a, uint8_t *smem, FbBars *bars) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   int q_fill = 0, do_fill = 0, own = 0;
   bool ok = true;
   for (int it = 0;; ++it) {
@@ -230,7 +223,7 @@ __device__ __forceinline__ bool fb_producer(const CUtensorMap *tq, const CUtenso
 
 // ----------------------------------------------------------------------------- MMA issuer
 __device__ __forceinline__ bool fb_mma(const FbArgs &a, uint8_t *smem, FbBars *bars, uint32_t tmem, int lane) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   const uint32_t k_s = smem_u32(smem + FB_SM_K), v_s = smem_u32(smem + FB_SM_V);
   const uint32_t q0_s = smem_u32(smem + FB_SM_Q), do_s = smem_u32(smem + FB_SM_DO);
   const uint32_t ds_s = smem_u32(smem + FB_SM_DS);
@@ -330,7 +323,7 @@ __device__ __forceinline__ bool fb_mma(const FbArgs &a, uint8_t *smem, FbBars *b
 // the readout of its columns of dQ^T.
 __device__ __forceinline__ bool fb_softmax(const CUtensorMap *tdq, const FbArgs &a, uint8_t *smem, FbBars *bars,
                                            uint32_t tmem, int w, int warp, int lane) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
   const uint32_t lane_off = uint32_t(quarter * 32) << 16;
@@ -517,20 +510,20 @@ __device__ __forceinline__ bool fb_softmax(const CUtensorMap *tdq, const FbArgs 
 // away, free TMEM, and let the last CTA reset the scheduler ticket.
 __device__ __forceinline__ void fb_finish(bool ok, const FbArgs &a, FbBars *bars, uint32_t tmem, int warp, int lane) {
   if (!ok) {
-    bars->abort = 1;
+    bars->ctl.abort = 1;
     raise_error(a.hdr + HDR_ERR, ERRBIT_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
-  if (bars->abort) {
+  if (bars->ctl.abort) {
     if (warp == FB_PRODUCER && lane == 0) {
-      for (int k = bars->q_use; k < bars->q_fill; ++k) fb_wait_plain(&bars->q_full[k & 1], (k >> 1) & 1);
-      for (int k = bars->do_use; k < bars->do_fill; ++k) fb_wait_plain(&bars->do_full, k & 1);
-      if (bars->own_issued > bars->own_used) fb_wait_plain(&bars->own_full, (bars->own_issued - 1) & 1);
+      for (int k = bars->q_use; k < bars->q_fill; ++k) bounded_wait_plain(&bars->q_full[k & 1], (k >> 1) & 1);
+      for (int k = bars->do_use; k < bars->do_fill; ++k) bounded_wait_plain(&bars->do_full, k & 1);
+      if (bars->own_issued > bars->own_used) bounded_wait_plain(&bars->own_full, (bars->own_issued - 1) & 1);
     }
     if (warp == FB_MMA && lane == 0) {
       mma_commit(&bars->drain);
-      fb_wait_plain(&bars->drain, 0);
+      bounded_wait_plain(&bars->drain, 0);
     }
     __syncthreads();
   }
@@ -577,7 +570,8 @@ __global__ void __launch_bounds__(FB_THREADS, 1)
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 1);
-    bars->abort = 0;
+    bars->ctl.abort = 0;
+    bars->ctl.limit_ns = pipeline_wait_limit(a.hdr);
     bars->q_fill = bars->q_use = bars->do_fill = bars->do_use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
   }
@@ -637,11 +631,10 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float4 *__restric
 cudaError_t launch_dkdvq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                          const CUtensorMap &tdqacc, void *dq, void *dk, void *dv, const Problem &p, void *workspace,
                          cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(dkdvq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FB_SMEM);
+  static std::atomic<uint64_t> attr_done{0};
+  {
+    const cudaError_t e = smem_attr_once(reinterpret_cast<const void *>(dkdvq_kernel), FB_SMEM, attr_done);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const Workspace w = Workspace::layout(p.B, p.S, p.H);
   char *base = static_cast<char *>(workspace);

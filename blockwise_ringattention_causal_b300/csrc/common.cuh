@@ -31,6 +31,7 @@ constexpr int ERRBIT_TIMEOUT = 2;
 enum HeaderWord {
   HDR_ERR = 0,          // error bits
   HDR_KV_CHUNK = 1,     // ring chunk length in key tiles
+  HDR_WAIT_LIMIT = 2,   // words 2-3: bound of the pipeline waits in ns (uint64; 0 = WAIT_LIMIT_NS)
   HDR_TICKET_FWD = 4,   // persistent-scheduler tickets and exit counters
   HDR_DONE_FWD = 5,
   HDR_TICKET_DKDV = 6,
@@ -151,20 +152,60 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase of `parity` to complete. Gives up (returns false) after
-// `limit_ns` of wall time or as soon as another role has raised *abort.
+// Bounded waiting. Every wait of a pipeline role gives up after `limit_ns` of wall
+// time (a phase that never completes would otherwise hang the GPU) or as soon as
+// another role of the CTA has raised `abort` after its own wait gave up. The kernels
+// then let copies and products in flight land, free TMEM and return; the host reads
+// the error word. limit_ns comes from the workspace header (HDR_WAIT_LIMIT, 0 = the
+// default below), so a test can shorten it and watch the waits run out.
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s: far above any legitimate wait
 
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+struct WaitCtl {
+  int abort;           // raised by the role whose wait ran out; the others poll it
+  int unused;
+  uint64_t limit_ns;   // bound of the pipeline waits
+};
+
+__device__ __forceinline__ uint64_t pipeline_wait_limit(const int *hdr) {
+  const uint64_t v = *reinterpret_cast<const uint64_t *>(hdr + HDR_WAIT_LIMIT);
+  return v ? v : WAIT_LIMIT_NS;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, WaitCtl *ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
+  const uint64_t limit = ctl->limit_ns;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+      if (*reinterpret_cast<volatile int *>(&ctl->abort)) return false;
+      if (global_timer_ns() - t0 > limit) return false;
     }
   }
+}
+
+// Spins (bounded like mbar_wait) until *count reaches target.
+__device__ __forceinline__ bool wait_count(volatile int *count, int target, WaitCtl *ctl) {
+  if (*count >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  const uint64_t limit = ctl->limit_ns;
+  for (uint32_t it = 1; *count < target; ++it) {
+    if ((it & 63u) == 0u) {
+      if (*reinterpret_cast<volatile int *>(&ctl->abort)) return false;
+      if (global_timer_ns() - t0 > limit) return false;
+    }
+  }
+  return true;
+}
+
+// Waits of the abort path (copies and products in flight must land before shared
+// memory and TMEM are released): always the full default bound, never the
+// configurable one.
+__device__ __forceinline__ bool bounded_wait_plain(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+  return true;
 }
 
 // ----------------------------------------------------------------------------- TMA

@@ -49,7 +49,7 @@ struct FwdBars {
   uint64_t drain;
   int item[2];
   uint32_t tmem_base;
-  int abort;
+  WaitCtl ctl;
   int kv_fill, kv_use_k, kv_use_v[2], q_issued, q_used;
   int s_issued[2];   // S products of query tile t issued so far
 };
@@ -131,7 +131,7 @@ __device__ __forceinline__ Ranges item_ranges(const FwdArgs &a, const Item &I) {
 // ----------------------------------------------------------------------------- producer
 __device__ bool producer_role(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                               const FwdArgs &a, uint8_t *smem, FwdBars *bars, int kv_chunk) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   int kv_fill = 0, q_issued = 0;
   bool ok = true;
   for (int it = 0;; ++it) {
@@ -182,7 +182,7 @@ __device__ bool producer_role(const CUtensorMap *tq, const CUtensorMap *tk, cons
 // tiles after the item's last product.
 __device__ bool s_issuer_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_t tmem, int kv_chunk,
                               int lane) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   const uint32_t kv_s0 = smem_u32(smem + SM_KV);
   int kv_use = 0, q_used = 0, n_s = 0, n_st[2] = {0, 0};
   bool ok = true;
@@ -236,19 +236,6 @@ __device__ bool s_issuer_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, ui
   return ok;
 }
 
-// Spins (bounded, like mbar_wait) until *count reaches target.
-__device__ __forceinline__ bool wait_count(volatile int *count, int target, volatile int *abort) {
-  if (*count >= target) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1; *count < target; ++it) {
-    if ((it & 63u) == 0u) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
-    }
-  }
-  return true;
-}
-
 // P.V issuer of query tile t: per key tile in ring order, O_t += P_t V once the softmax
 // has written P_t and rescaled O_t, then its share of the V stage's release. The first
 // product of an item overwrites O_t once the previous item's O_t has been read out.
@@ -257,7 +244,7 @@ __device__ __forceinline__ bool wait_count(volatile int *count, int target, vola
 // per tile, so that neither tile's P.V waits for the other's S.
 __device__ bool pv_issuer_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, uint32_t tmem, int kv_chunk,
                                int t, int lane) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   volatile int *s_issued = bars->s_issued + t;
   const uint32_t kv_s0 = smem_u32(smem + SM_KV);
   int kv_use = 0, n_pv = 0;
@@ -312,7 +299,7 @@ __device__ bool pv_issuer_role(const FwdArgs &a, uint8_t *smem, FwdBars *bars, u
 // ----------------------------------------------------------------------------- softmax
 __device__ bool softmax_role(const FwdArgs &a, FwdBars *bars, uint32_t tmem, int kv_chunk, int t, int warp,
                              int lane) {
-  volatile int *abort = &bars->abort;
+  WaitCtl *abort = &bars->ctl;
   const int wq = warp & 3;
   const int r = wq * 32 + lane;
   const uint32_t lane_off = uint32_t(wq * 32) << 16;
@@ -472,13 +459,6 @@ __device__ bool softmax_role(const FwdArgs &a, FwdBars *bars, uint32_t tmem, int
   return ok;
 }
 
-__device__ bool bounded_wait_plain(uint64_t *bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
-  return true;
-}
-
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
@@ -505,7 +485,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       mbar_init(&bars->item_empty[t], 11);   // softmax 8 + MMA 3 warps
     }
     mbar_init(&bars->drain, 3);
-    bars->abort = 0;
+    bars->ctl.abort = 0;
+    bars->ctl.limit_ns = pipeline_wait_limit(a.hdr);
     bars->kv_fill = bars->kv_use_k = bars->kv_use_v[0] = bars->kv_use_v[1] = bars->q_issued = bars->q_used = 0;
     bars->s_issued[0] = bars->s_issued[1] = 0;
     fence_mbar_init();
@@ -536,12 +517,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     ok = softmax_role(a, bars, tmem, kv_chunk, warp >> 2, warp, lane);
   }
   if (!ok) {
-    bars->abort = 1;
+    bars->ctl.abort = 1;
     raise_error(a.hdr + HDR_ERR, ERRBIT_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
-  if (bars->abort) {
+  if (bars->ctl.abort) {
     // Let copies and MMAs still in flight land before shared memory and TMEM go away.
     if (warp == WARP_PRODUCER && lane == 0) {
       // loads no consumer has waited for: K (even n) from the S issuer's count, V (odd n)
@@ -577,11 +558,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, void *out,
                        float *lse, const Problem &p, void *workspace, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
+  static std::atomic<uint64_t> attr_done{0};
+  {
+    const cudaError_t e = smem_attr_once(reinterpret_cast<const void *>(fwd_kernel), FWD_SMEM, attr_done);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const Workspace w = Workspace::layout(p.B, p.S, p.H);
   char *base = static_cast<char *>(workspace);

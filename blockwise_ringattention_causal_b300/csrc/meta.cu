@@ -136,7 +136,8 @@ __device__ __forceinline__ int range_size(const int *lr, int S, int q0) {
 //   list 0: forward query-tile pairs (b, p)  - cost = key tiles of both tiles;
 //   list 1: key tiles (b, kt) for dK/dV     - cost = query tiles that see the tile;
 //   list 2: query tiles (b, qt) for dQ      - cost = key tiles the tile needs.
-// Items of equal cost keep no particular order. The block also resets the tickets.
+// Items of equal cost (or, for costs above NBINS, of costs that share a bin) keep no
+// particular order. The block also resets the tickets.
 __global__ void __launch_bounds__(META_THREADS) meta_sort_kernel(const int *__restrict__ lo,
                                                                  const int *__restrict__ kend, int B, int S,
                                                                  int S_pad, int nT, int nP, int *__restrict__ hdr,
@@ -169,8 +170,20 @@ __global__ void __launch_bounds__(META_THREADS) meta_sort_kernel(const int *__re
       return range_size(lo + size_t(idx / nT) * S_pad, S, (idx % nT) * BM);
     }
   };
+  // Costs reach 2 * nT (16384 key tiles for a forward pair at S = 1M), more than there
+  // are bins: scale them by the smallest integer that maps the largest onto the bins,
+  // so that the list stays longest first (items within one bin: any order).
+  int cmax = 0;
+  for (int idx = threadIdx.x; idx < n; idx += META_THREADS) cmax = max(cmax, cost_of(idx));
+  for (int d = 16; d > 0; d >>= 1) cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, d));
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = cmax;
+  __syncthreads();
+  cmax = 0;
+  for (int k = 0; k < META_THREADS / 32; ++k) cmax = max(cmax, scratch[k]);
+  __syncthreads();
+  const int div = cmax / NBINS + 1;   // cmax / div <= NBINS - 1
   // bins in descending cost order: bin 0 holds the largest costs
-  auto bin_of = [&](int c) -> int { return NBINS - 1 - min(c, NBINS - 1); };
+  auto bin_of = [&](int c) -> int { return NBINS - 1 - c / div; };
 
   for (int idx = threadIdx.x; idx < n; idx += META_THREADS) atomicAdd(&hist[bin_of(cost_of(idx))], 1);
   __syncthreads();

@@ -9,7 +9,9 @@
 //
 // The array is a host-side stand-in in host code: its address on a device is fetched
 // with cudaGetSymbolAddress once per device (with that device current) and passed to
-// the kernels like any caller-provided workspace.
+// the kernels like any caller-provided workspace. The cached address belongs to the
+// runtime's primary context of that device: it assumes that context lives as long as
+// the process (no cudaDeviceReset in between, no other context made current).
 #include <cstdio>
 #include <mutex>
 
@@ -52,11 +54,8 @@ extern "C" lwm_status lwm_attn_fwd_noalloc(const lwm_bf16 *q, const lwm_bf16 *k,
                                            const int32_t *seg_ids, const int32_t *pos, lwm_bf16 *out,
                                            float *lse, int B, int S, int H, int D, lwm_stream stream) {
   using namespace lwm;
-  if (B <= 0 || S <= 0 || H <= 0 || D <= 0) return LWM_ERR_INVALID_ARG;
-  if (D != HD) return LWM_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * S >= (1ll << 31)) return LWM_ERR_INVALID_ARG;
-  const long long nT = (S + BM - 1) / BM;
-  if (static_cast<long long>(B) * ((nT + 1) / 2) * H >= (1ll << 31)) return LWM_ERR_INVALID_ARG;
+  const lwm_status sz = check_sizes(B, S, H, D);
+  if (sz != LWM_OK) return sz;
   // The forward pass uses only the part of the workspace in front of the backward
   // rows; its size does not depend on H, and the layout with H = 1 (without the dQ
   // accumulator of the backward pass) covers it.
@@ -66,6 +65,9 @@ extern "C" lwm_status lwm_attn_fwd_noalloc(const lwm_bf16 *q, const lwm_bf16 *k,
   const auto a4 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
   if (!a16(q) || !a16(k) || !a16(v) || !a16(out) || !a4(lse)) return LWM_ERR_ALIGNMENT;
   if ((seg_ids && !a4(seg_ids)) || (pos && !a4(pos))) return LWM_ERR_ALIGNMENT;
+  // an unsupported device is reported as such before the array is looked up
+  const lwm_status dev = check_device();
+  if (dev != LWM_OK) return dev;
   void *scratch = nullptr;
   const lwm_status st = noalloc_scratch(&scratch);
   if (st != LWM_OK) return st;

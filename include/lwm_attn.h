@@ -189,8 +189,11 @@ lwm_status lwm_attn_bwd_stages(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_b
  *     on the GPU (different streams, or several host threads) race on the array and
  *     must be serialised by the caller.
  *   - Errors: argument errors are returned as by lwm_attn_fwd. Device-side conditions
- *     (seg_ids / pos that break the preconditions) are not reported, because the error
- *     word lives in the shared array; the outputs for such inputs are undefined. */
+ *     (seg_ids / pos that break the preconditions, and a bounded pipeline wait that ran
+ *     out) are not reported, because the error word lives in the shared array and no
+ *     call returns it; the outputs of such a call are undefined.
+ *   - Context: the cached address belongs to the device's primary runtime context; it
+ *     assumes that context lives as long as the process (no cudaDeviceReset). */
 lwm_status lwm_attn_fwd_noalloc(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v,
                                 const int32_t *seg_ids, const int32_t *pos, lwm_bf16 *out, float *lse,
                                 int B, int S, int H, int D, lwm_stream stream);
@@ -199,6 +202,21 @@ lwm_status lwm_attn_fwd_noalloc(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_
  * `workspace` (LWM_OK, LWM_ERR_SEGMENTS or LWM_ERR_TIMEOUT), or LWM_ERR_CUDA if the
  * stream reported a CUDA error. */
 lwm_status lwm_attn_check(void *workspace, lwm_stream stream);
+
+/* Bound of the kernels' pipeline waits, for tests of the failure path. Every wait of a
+ * kernel role on another role (an mbarrier phase, a counter) gives up after a bound of
+ * wall time, sets LWM_ERR_TIMEOUT in the workspace's error word, and the kernel lets
+ * copies and products in flight land, frees its tensor memory and returns, so the
+ * CUDA context stays usable. The default bound is 2 s, far above any legitimate wait.
+ * This call stores `limit_ns` in `workspace` (enqueued on `stream`; 0 restores the
+ * default); every later call with that workspace uses it until it is changed. A limit
+ * of a few microseconds makes the waits run out on purpose: a test can then check that
+ * lwm_attn_check() returns LWM_ERR_TIMEOUT and that the next call with the default
+ * bound still computes correct results. The waits that let in-flight work land keep
+ * the default bound. Source: none on the LWM pages (failure handling of this
+ * library). Returns LWM_ERR_INVALID_ARG for a NULL workspace, LWM_ERR_WORKSPACE for a
+ * workspace that is not 256-byte aligned, LWM_ERR_CUDA if the launch fails. */
+lwm_status lwm_attn_set_wait_limit(void *workspace, uint64_t limit_ns, lwm_stream stream);
 
 /* Description of the most recent LWM_ERR_CUDA raised on the calling host thread: the
  * failing call and the CUDA error text ("" if none). The string is owned by the

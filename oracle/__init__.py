@@ -25,5 +25,7 @@ from .attention import (  # noqa: F401
     attention_forward_rows,
     attention_backward_rows,
     attention_key_grads,
+    forward_row_block,
+    backward_row_block,
     credited_pairs,
 )

@@ -31,9 +31,10 @@ Rows with seg < 0 (padding) see nothing: o = 0, lse = -inf, and they add nothing
 any gradient. The softmax scale is fixed at 1/sqrt(D).
 
 Only the rows are processed in chunks, to bound memory: each query row is still the
-plain, whole-row softmax of its definition, and only keys j <= max(row) of a chunk
-are formed because every other key is outside every V(i) of the chunk. No online
-softmax, blocking over keys or reordering is used here.
+plain, whole-row softmax of its definition. Of the keys, a chunk forms only the
+window [j0, max(row)] outside which the mask shows no visible key for any of its rows
+(p = 0 there, exactly). No online softmax, blocking over keys or reordering is used
+here.
 
 Layouts: q, k, v, dout are [B, S, H, D]; seg is [B, S]; lse is returned as [B, H, S].
 Inputs are converted to float64 (callers pass the bf16-rounded values so that both
@@ -67,11 +68,19 @@ def visible_mask(seg_row, rows):
 def _rows_softmax(q_bh, k_bh, seg_row, rows, scale):
     """Scores, probabilities and lse for query rows ``rows`` of one (b, h).
 
-    Returns (p [R, J], lse [R], J) where J = max(rows) + 1 keys are formed.
+    ``q_bh`` and ``k_bh`` are [S, D] (any float type; the rows used are taken to float64).
+
+    Returns (p [R, J - j0], lse [R], j0, J): J = max(rows) + 1, and [j0, J) holds every
+    key that the mask makes visible from at least one of the rows (the first such key
+    is j0; keys outside that window are invisible from every row, so their p is 0 and
+    they are not formed). p[:, c] belongs to key j0 + c.
     """
     J = int(rows.max()) + 1
     mask = visible_mask(seg_row[:J], rows) if J > 0 else np.zeros((len(rows), 0), bool)
-    s = (q_bh[rows] @ k_bh[:J].T) * scale
+    cols = mask.any(axis=0)
+    j0 = int(np.argmax(cols)) if cols.any() else J
+    mask = mask[:, j0:]
+    s = (_f64(q_bh[rows]) @ _f64(k_bh[j0:J]).T) * scale
     s = np.where(mask, s, -np.inf)
     has = mask.any(axis=1)
     m = np.where(has, np.max(s, axis=1, initial=-np.inf), 0.0)
@@ -82,7 +91,13 @@ def _rows_softmax(q_bh, k_bh, seg_row, rows, scale):
     lse[has] = m[has] + np.log(l[has])
     p = np.zeros_like(s)
     p[has] = e[has] / l[has][:, None]
-    return p, lse, J
+    return p, lse, j0, J
+
+
+def _chunk_rows(n_keys):
+    """Rows per chunk: at most ROW_CHUNK, and few enough that a chunk's score matrix over
+    ``n_keys`` keys holds at most 2^24 entries (memory only; every row is independent)."""
+    return max(16, min(ROW_CHUNK, (1 << 24) // max(int(n_keys), 1)))
 
 
 def _chunks(rows, size=ROW_CHUNK):
@@ -90,49 +105,66 @@ def _chunks(rows, size=ROW_CHUNK):
         yield rows[c:c + size]
 
 
+def _seg_or_zeros(seg, B, S):
+    return np.zeros((B, S), np.int64) if seg is None else np.asarray(seg)
+
+
+def forward_row_block(q, k, v, seg, b, h, rows):
+    """out [R, D] and lse [R] of query rows ``rows`` of (b, h): the whole-row softmax of
+    each row (the body of :func:`attention_forward`)."""
+    B, S, H, D = np.shape(q)
+    seg_row = _seg_or_zeros(seg, B, S)[b]
+    rows = np.asarray(rows, dtype=np.int64)
+    p, lse, j0, J = _rows_softmax(q[b, :, h], k[b, :, h], seg_row, rows, 1.0 / np.sqrt(D))
+    return p @ _f64(v[b, j0:J, h]), lse
+
+
+def backward_row_block(q, k, v, dout, seg, b, h, rows):
+    """Gradient terms of query rows ``rows`` of (b, h) (the body of :func:`attention_backward`).
+
+    Returns (dq [R, D], j0, dk_part [J - j0, D], dv_part [J - j0, D]): dq of those rows,
+    and their terms of dk_j and dv_j for keys j0 <= j < J (no other key gets any from
+    these rows). dk and dv are the sums of these terms over all row blocks.
+    """
+    B, S, H, D = np.shape(q)
+    seg_row = _seg_or_zeros(seg, B, S)[b]
+    rows = np.asarray(rows, dtype=np.int64)
+    scale = 1.0 / np.sqrt(D)
+    p, _, j0, J = _rows_softmax(q[b, :, h], k[b, :, h], seg_row, rows, scale)
+    kw, vw = _f64(k[b, j0:J, h]), _f64(v[b, j0:J, h])
+    do = _f64(dout[b, rows, h])
+    dp = do @ vw.T
+    delta = np.sum(p * dp, axis=1)
+    ds = p * (dp - delta[:, None])
+    return scale * (ds @ kw), j0, scale * (ds.T @ _f64(q[b, rows, h])), p.T @ do
+
+
 def attention_forward(q, k, v, seg=None):
     """Full forward pass: returns (out [B,S,H,D], lse [B,H,S]) in float64."""
-    q, k, v = _f64(q), _f64(k), _f64(v)
-    B, S, H, D = q.shape
-    if seg is None:
-        seg = np.zeros((B, S), np.int64)
-    seg = np.asarray(seg)
-    scale = 1.0 / np.sqrt(D)
+    B, S, H, D = np.shape(q)
     out = np.zeros((B, S, H, D))
     lse = np.full((B, H, S), -np.inf)
-    rows_all = np.arange(S)
     for b in range(B):
         for h in range(H):
-            for rows in _chunks(rows_all):
-                p, l, J = _rows_softmax(q[b, :, h], k[b, :, h], seg[b], rows, scale)
-                out[b, rows, h] = p @ v[b, :J, h]
-                lse[b, h, rows] = l
+            for rows in _chunks(np.arange(S), _chunk_rows(S)):
+                out[b, rows, h], lse[b, h, rows] = forward_row_block(q, k, v, seg, b, h, rows)
     return out, lse
 
 
 def attention_backward(q, k, v, dout, seg=None):
     """Full gradients (dq, dk, dv), each [B,S,H,D] float64, for L = sum(dout * out)."""
-    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
-    B, S, H, D = q.shape
-    if seg is None:
-        seg = np.zeros((B, S), np.int64)
-    seg = np.asarray(seg)
-    scale = 1.0 / np.sqrt(D)
-    dq = np.zeros_like(q)
-    dk = np.zeros_like(k)
-    dv = np.zeros_like(v)
-    rows_all = np.arange(S)
+    B, S, H, D = np.shape(q)
+    dq = np.zeros((B, S, H, D))
+    dk = np.zeros((B, S, H, D))
+    dv = np.zeros((B, S, H, D))
     for b in range(B):
         for h in range(H):
-            for rows in _chunks(rows_all):
-                p, _, J = _rows_softmax(q[b, :, h], k[b, :, h], seg[b], rows, scale)
-                do = dout[b, rows, h]
-                dp = do @ v[b, :J, h].T
-                delta = np.sum(p * dp, axis=1)
-                ds = p * (dp - delta[:, None])
-                dq[b, rows, h] = scale * (ds @ k[b, :J, h])
-                dk[b, :J, h] += scale * (ds.T @ q[b, rows, h])
-                dv[b, :J, h] += p.T @ do
+            for rows in _chunks(np.arange(S), _chunk_rows(S)):
+                g, j0, gk, gv = backward_row_block(q, k, v, dout, seg, b, h, rows)
+                J = j0 + gk.shape[0]
+                dq[b, rows, h] = g
+                dk[b, j0:J, h] += gk
+                dv[b, j0:J, h] += gv
     return dq, dk, dv
 
 
@@ -145,19 +177,11 @@ def attention_forward_rows(q, k, v, seg, b, rows, heads=None):
     B, S, H, D = np.shape(q)
     heads = list(range(H)) if heads is None else list(heads)
     rows = np.asarray(rows, dtype=np.int64)
-    seg_row = np.zeros(S, np.int64) if seg is None else np.asarray(seg)[b]
-    scale = 1.0 / np.sqrt(D)
     out = np.zeros((len(rows), len(heads), D))
     lse = np.zeros((len(heads), len(rows)))
     for hi, h in enumerate(heads):
-        qh, kh, vh = _f64(q[b, :, h]), None, None
-        J = int(rows.max()) + 1
-        kh = _f64(k[b, :J, h])
-        vh = _f64(v[b, :J, h])
         for idx in _chunks(np.arange(len(rows)), 256):
-            p, l, Jc = _rows_softmax(qh, kh, seg_row, rows[idx], scale)
-            out[idx, hi] = p @ vh[:Jc]
-            lse[hi, idx] = l
+            out[idx, hi], lse[hi, idx] = forward_row_block(q, k, v, seg, b, h, rows[idx])
     return out, lse
 
 
@@ -169,54 +193,43 @@ def attention_backward_rows(q, k, v, dout, seg, b, rows, heads=None):
     B, S, H, D = np.shape(q)
     heads = list(range(H)) if heads is None else list(heads)
     rows = np.asarray(rows, dtype=np.int64)
-    seg_row = np.zeros(S, np.int64) if seg is None else np.asarray(seg)[b]
-    scale = 1.0 / np.sqrt(D)
     dq = np.zeros((len(rows), len(heads), D))
-    J = int(rows.max()) + 1
     for hi, h in enumerate(heads):
-        qh = _f64(q[b, :, h])
-        kh = _f64(k[b, :J, h])
-        vh = _f64(v[b, :J, h])
         for idx in _chunks(np.arange(len(rows)), 256):
-            r = rows[idx]
-            p, _, Jc = _rows_softmax(qh, kh, seg_row, r, scale)
-            do = _f64(dout[b, r, h])
-            dp = do @ vh[:Jc].T
-            delta = np.sum(p * dp, axis=1)
-            ds = p * (dp - delta[:, None])
-            dq[idx, hi] = scale * (ds @ kh[:Jc])
+            dq[idx, hi] = backward_row_block(q, k, v, dout, seg, b, h, rows[idx])[0]
     return dq
 
 
-def attention_key_grads(q, k, v, dout, seg, b, h, keys):
+def attention_key_grads(q, k, v, dout, seg, b, h, keys, row_range=None):
     """(dk [K, D], dv [K, D]) for selected keys of batch row ``b``, head ``h``.
 
     dk_j and dv_j sum over every query that sees key j, and each term needs that
-    query's whole-row softmax, so every row i >= min(keys) is formed in full.
+    query's whole-row softmax (and its delta), so every row i >= min(keys) is formed
+    in full; only the selected keys' columns of ds and p enter the sums.
+    ``row_range`` = (r0, r1) restricts the sum to queries r0 <= i < r1 (a part of the
+    sum; the parts over disjoint ranges add up to the whole).
     """
     B, S, H, D = np.shape(q)
     keys = np.asarray(keys, dtype=np.int64)
-    seg_row = np.zeros(S, np.int64) if seg is None else np.asarray(seg)[b]
+    seg_row = _seg_or_zeros(seg, B, S)[b]
     scale = 1.0 / np.sqrt(D)
-    qh = _f64(q[b, :, h])
-    kh = _f64(k[b, :, h])
-    vh = _f64(v[b, :, h])
-    doh = _f64(dout[b, :, h])
+    start, stop = (int(keys.min()), S) if row_range is None else (max(int(keys.min()), row_range[0]), row_range[1])
     dk = np.zeros((len(keys), D))
     dv = np.zeros((len(keys), D))
-    start = int(keys.min())
-    for rows in _chunks(np.arange(start, S)):
-        p, _, J = _rows_softmax(qh, kh, seg_row, rows, scale)
-        do = doh[rows]
-        dp = do @ vh[:J].T
-        delta = np.sum(p * dp, axis=1)
-        sel = keys < J
+    if stop <= start:
+        return dk, dv
+    for rows in _chunks(np.arange(start, stop), _chunk_rows(stop)):
+        p, _, j0, J = _rows_softmax(q[b, :, h], k[b, :, h], seg_row, rows, scale)
+        sel = (keys >= j0) & (keys < J)
         if not sel.any():
             continue
-        kk = keys[sel]
-        ps = p[:, kk]
-        ds = ps * (dp[:, kk] - delta[:, None])
-        dk[sel] += scale * (ds.T @ qh[rows])
+        do = _f64(dout[b, rows, h])
+        dp = do @ _f64(v[b, j0:J, h]).T
+        delta = np.sum(p * dp, axis=1)
+        cols = keys[sel] - j0
+        ps = p[:, cols]
+        ds = ps * (dp[:, cols] - delta[:, None])
+        dk[sel] += scale * (ds.T @ _f64(q[b, rows, h]))
         dv[sel] += ps.T @ do
     return dk, dv
 

@@ -13,6 +13,7 @@ import torch
 import blockwise_ringattention_causal_b300 as lwm
 from blockwise_ringattention_causal_b300 import inputs as I
 import oracle
+from tests._oracle_pool import OraclePool
 from tests._parity import GRAD_REL, f64, rel_l2
 
 pytestmark = pytest.mark.gpu
@@ -140,8 +141,8 @@ def test_video_s256k_sampled_and_invariants(cuda_device):
     """256K tokens (1024 frames of 256 tokens with a shared per-frame offset).
 
     dq on 512 sampled query rows of a subset of heads (exact from each row alone); dk, dv
-    on the last 256 keys of two heads (exact from the rows that see them); and on every
-    head the identities that hold at any size: sum_j dv_j = sum_i dout_i (each row's
+    on the last 256 keys of two heads and on 256 keys of the first four frames of two
+    heads (exact from every row that sees them); and on every head the identities that hold at any size: sum_j dv_j = sum_i dout_i (each row's
     probabilities sum to 1) and sum_j dk_j = 0 (each row's dS sums to 0).
     """
     w = I.workload(4)
@@ -167,6 +168,18 @@ def test_video_s256k_sampled_and_invariants(cuda_device):
     e_dk = rel_l2(np.concatenate(gk), np.concatenate(rk))
     e_dv = rel_l2(np.concatenate(gv), np.concatenate(rv))
     assert max(e_dq, e_dk, e_dv) <= GRAD_REL, f"dq {e_dq:.2e} dk {e_dk:.2e} dv {e_dv:.2e}"
+    # 256 early keys (frames 0-3) of two heads: each column sums over ~262K queries, the
+    # long accumulations of the persistent dK/dV kernel; the oracle forms every row
+    early = np.sort(np.random.default_rng(4).choice(4 * I.FRAME_TOKENS, 256, replace=False))
+    heads = (4, 22)
+    tensors = {n: x[n][:, :, list(heads)].float().cpu().numpy() for n in ("q", "k", "v", "dout")}
+    with OraclePool(tensors, seg) as pool:
+        ref = pool.key_grads(0, [0, 1], early)
+    gk = np.stack([f64(dk[0, early, h]) for h in heads])
+    gv = np.stack([f64(dv[0, early, h]) for h in heads])
+    e_dk = rel_l2(gk, np.stack([ref[i][0] for i in range(2)]))
+    e_dv = rel_l2(gv, np.stack([ref[i][1] for i in range(2)]))
+    assert max(e_dk, e_dv) <= GRAD_REL, f"early keys: dk {e_dk:.2e} dv {e_dv:.2e}"
     # identities over all heads, in float64 on the device
     sum_dv = dv[0].double().sum(dim=0)            # [H, D]
     sum_do = x["dout"][0].double().sum(dim=0)

@@ -141,7 +141,7 @@ def test_packed_mixed_s64k_sampled_rows(cuda_device):
 # The whole-row oracle is exact but costs O(rows x S x D) host flops per head, so at
 # S >= 256K it runs on 512 sampled query rows of a spread subset of heads.
 SAMPLED_HEADS_256K = (0, 9, 18, 27)
-SAMPLED_HEADS_1M = (0, 21)
+SAMPLED_HEADS_1M = (0, 10, 21, 31)
 
 
 def _sampled_heads(w, x, out, lse, heads, rows_per_call):

@@ -301,6 +301,20 @@ def test_sampled_rows_and_keys_match_full():
             kk, vv = oracle.attention_key_grads(q, k, v, do, seg, b, h, rows)
             np.testing.assert_allclose(kk, dk[b, rows, h], atol=1e-13)
             np.testing.assert_allclose(vv, dv[b, rows, h], atol=1e-13)
+            # the sum over queries split into disjoint query ranges adds up to the whole
+            parts = [oracle.attention_key_grads(q, k, v, do, seg, b, h, rows, row_range=r)
+                     for r in ((0, 70), (70, 260), (260, S))]
+            np.testing.assert_allclose(sum(p[0] for p in parts), kk, atol=1e-13)
+            np.testing.assert_allclose(sum(p[1] for p in parts), vv, atol=1e-13)
+            # the row-block terms of the full backward add up to dq, dk, dv
+            gk, gv = np.zeros((S, D)), np.zeros((S, D))
+            for r in (np.arange(0, 37), np.arange(37, 180), np.arange(180, S)):
+                g, j0, pk, pv = oracle.backward_row_block(q, k, v, do, seg, b, h, r)
+                np.testing.assert_allclose(g, dq[b, r, h], atol=1e-13)
+                gk[j0:j0 + len(pk)] += pk
+                gv[j0:j0 + len(pv)] += pv
+            np.testing.assert_allclose(gk, dk[b, :, h], atol=1e-13)
+            np.testing.assert_allclose(gv, dv[b, :, h], atol=1e-13)
 
 
 def test_credited_pairs_counts_the_visible_set():
@@ -354,9 +368,9 @@ def test_planted_gradient_mistake_is_caught():
     scale = 1.0 / math.sqrt(D)
     dq_bad = np.zeros_like(q)
     for i in range(S):                                   # planted: ds = p * dp (no delta)
-        p, _, J = OA._rows_softmax(q[0, :, 0], k[0, :, 0], seg[0], np.array([i]), scale)
-        dp = do[0, i, 0] @ v[0, :J, 0].T
-        dq_bad[0, i, 0] = scale * ((p * dp) @ k[0, :J, 0])[0]
+        p, _, j0, J = OA._rows_softmax(q[0, :, 0], k[0, :, 0], seg[0], np.array([i]), scale)
+        dp = do[0, i, 0] @ v[0, j0:J, 0].T
+        dq_bad[0, i, 0] = scale * ((p * dp) @ k[0, j0:J, 0])[0]
     h = 1e-6
     num = np.zeros_like(q)
     for idx in np.ndindex(q.shape):
