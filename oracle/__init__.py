@@ -29,3 +29,15 @@ from .attention import (  # noqa: F401
     backward_row_block,
     credited_pairs,
 )
+from .rope import (  # noqa: F401
+    rope_angles,
+    rope_rotate,
+    round_bf16,
+    attention_forward_rope,
+    attention_backward_rope,
+)
+from .loss_weighting import (  # noqa: F401
+    documents,
+    token_cross_entropy,
+    packed_loss,
+)
