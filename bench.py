@@ -31,7 +31,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "causal attn TFLOP/s (fwd, fwd+bwd) at S=32K–1M on 1 B300; % of BF16 dense peak"
-DATASHEET_BF16_TFLOPS = 2250.0   # dense bf16 per GPU (NVIDIA's figures halved for 2:4 sparsity)
+# NVIDIA's published HGX B300 figure is 36 PFLOP/s FP16/BF16 for 8 GPUs with 2:4 sparsity:
+# 4.5 PFLOP/s sparse, 2.25 PFLOP/s dense per GPU.
+DATASHEET_BF16_TFLOPS = 2250.0
 
 
 def load_peaks():
@@ -353,6 +355,15 @@ def run_ours(args, rank, world):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
         del dev_in
 
+    extras = {}
+    if not args.no_extras:
+        del x, q, k, v, dout, out, lse
+        if w.backward:
+            del dq, dk, dv
+        del ws
+        torch.cuda.empty_cache()
+        extras = run_extras(args, dev, stream, peaks, value if w.name == "causal-S32K-H32-D128" else None)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         S_sample, heads = 8192, 8
@@ -376,8 +387,144 @@ def run_ours(args, rank, world):
                             "datasheet_dense": 100 * value / DATASHEET_BF16_TFLOPS},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+            **extras,
         }
         print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- further kernels
+def _time(fn, steps, warmup, stream):
+    """Mean ms per call of fn() over `steps` calls after `warmup`, CUDA events on `stream`."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def run_extras(args, dev, stream, peaks, value_32k):
+    """The packed mixed-modality workload's fwd+bwd, and the memory-bound kernels of the
+    path (RoPE, decoding against a 1M-token cache, the re-weighted packed loss), each
+    timed alone on its own inputs (not inside the headline's timed region)."""
+    import blockwise_ringattention_causal_b300 as lwm
+    from blockwise_ringattention_causal_b300 import inputs as I
+    out = {}
+    steps, warmup = max(3, min(args.steps, 10)), 3
+    hbm = peaks["hbm"]
+
+    # packed mixed modality: B = 2 rows of 64K tokens, 19 + 25 documents
+    w = I.workload(3)
+    x = I.make_inputs(w, dev)
+    B, S, H, D = w.B, w.S, w.H, w.D
+    o = torch.empty_like(x["q"])
+    l = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
+    ws = lwm.new_workspace(B, S, H, D, dev, forward_only=True)
+    evs = []
+
+    def packed_step(record=False):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if record else None
+        if e: e[0].record(stream)
+        lwm.lwm_attn_prepare(x["seg"], x["pos"], B, S, H, D, 1, ws, stream)
+        if e: e[1].record(stream)
+        lwm.lwm_attn_fwd_prepared(x["q"], x["k"], x["v"], o, l, ws, stream)
+        if e: e[2].record(stream)
+        lwm.lwm_attn_bwd_stages(None, None, None, o, x["dout"], l, None, None, None, lwm.LWM_BWD_DELTA, ws, stream)
+        if e: e[3].record(stream)
+        lwm.lwm_attn_bwd_stages(x["q"], x["k"], x["v"], None, x["dout"], None, None, dk, dv, lwm.LWM_BWD_DKDV, ws,
+                                stream)
+        if e: e[4].record(stream)
+        lwm.lwm_attn_bwd_stages(x["q"], x["k"], x["v"], None, x["dout"], None, dq, None, None, lwm.LWM_BWD_DQ, ws,
+                                stream)
+        if e:
+            e[5].record(stream)
+            evs.append(e)
+
+    ms = _time(lambda: packed_step(True), steps, warmup, stream)
+    evs[:] = evs[warmup:]
+    if lwm.lwm_attn_check(ws) != 0:
+        raise RuntimeError("device error in the packed workload")
+    pairs = I.pairs_per_head(w)
+    names = ["meta", "fwd", "delta", "dkdv", "dq"]
+    kms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, n in enumerate(names)}
+    pv = 14.0 * D * H * pairs / (ms * 1e-3) / 1e12
+    out["packed"] = {"workload": w.name, "value": pv, "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
+                     "credited_pairs_per_head": pairs, "fwd_tflops": 4.0 * D * H * pairs / (kms["fwd"] * 1e-3) / 1e12,
+                     "kernel_ms": {n: round(t, 4) for n, t in kms.items()},
+                     "ratio_to_causal_32k": (pv / value_32k) if value_32k else None}
+
+    # RoPE on q and k of the 32K workload (theta = 1e6, LWM's 32K stage): read q, k and
+    # pos, write the rotated q, k
+    w2 = I.workload(2)
+    B, S, H = w2.B, w2.S, w2.H
+    del x, o, l, dq, dk, dv, ws
+    torch.cuda.empty_cache()
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    q = torch.randn((B, S, H, D), generator=g, device=dev, dtype=torch.bfloat16)
+    k = torch.randn((B, S, H, D), generator=g, device=dev, dtype=torch.bfloat16)
+    pos = torch.arange(S, dtype=torch.int32, device=dev).repeat(B, 1).contiguous()
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+    ms = _time(lambda: lwm.lwm_attn_rope(q, k, pos, 1e6, qr, kr, False, stream), steps, warmup, stream)
+    nbytes = 4 * B * S * H * D * 2 + B * S * 4
+    out["rope"] = {"shape": [B, S, H, D], "theta": 1e6, "ms": ms, "bytes": nbytes,
+                   "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                                "frac": nbytes / (ms * 1e-3) / 1e9 / hbm}}
+    del q, k, qr, kr, pos
+    torch.cuda.empty_cache()
+
+    # decoding: T new tokens of one row against a 2^20-token cache, 32 heads
+    Sd = 1 << 18 if args.extras_small else 1 << 20
+    kc = torch.randn((1, Sd, H, D), generator=g, device=dev, dtype=torch.bfloat16)
+    vc = torch.randn((1, Sd, H, D), generator=g, device=dev, dtype=torch.bfloat16)
+    dec = {}
+    for T in (1, 4):
+        qd = torch.randn((1, T, H, D), generator=g, device=dev, dtype=torch.bfloat16)
+        od = torch.empty_like(qd)
+        ld = torch.empty((1, H, T), dtype=torch.float32, device=dev)
+        wsd = torch.zeros(lwm.lwm_attn_decode_workspace_size(1, T, Sd, H, D), dtype=torch.uint8, device=dev)
+        ms = _time(lambda: lwm.lwm_attn_decode(qd, kc, vc, None, od, ld, wsd, stream), steps, warmup, stream)
+        if lwm.lwm_attn_check(wsd) != 0:
+            raise RuntimeError("device error in decoding")
+        nbytes = 2 * Sd * H * D * 2 + 2 * T * H * D * 2
+        dec[f"T{T}"] = {"ms": ms, "bytes": nbytes,
+                        "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": hbm,
+                                     "unit": "GB/s", "frac": nbytes / (ms * 1e-3) / 1e9 / hbm}}
+    out["decode"] = {"cache_tokens": Sd, "heads": H, **dec}
+    del kc, vc
+    torch.cuda.empty_cache()
+
+    # the re-weighted packed loss over the packed workload's rows, vocabulary 32768
+    if args.extras_small:
+        w = I.custom(1, 16384, 1, 128, [[4000, 258, 9000, 258, 2868]], name="packed-16K")
+    Bl, Sl, V = w.B, w.S, 32768
+    seg_np, _ = I.segments(w)
+    seg = torch.from_numpy(seg_np).to(dev)
+    logits = (torch.randn((Bl, Sl, V), generator=g, device=dev) * 2).to(torch.bfloat16)
+    targets = torch.randint(0, V, (Bl, Sl), generator=g, device=dev, dtype=torch.int32)
+    wt = torch.ones((Bl, Sl), dtype=torch.float32, device=dev)
+    for b, lens in enumerate(w.lengths):
+        ends = torch.tensor([sum(lens[:i + 1]) - 1 for i in range(len(lens))], device=dev)
+        wt[b, ends] = 0.0
+    loss = torch.empty(1, dtype=torch.float64, device=dev)
+    dlog = torch.empty_like(logits)
+    wsl = torch.zeros(lwm.lwm_packed_loss_workspace_size(Bl, Sl), dtype=torch.uint8, device=dev)
+    ms = _time(lambda: lwm.lwm_packed_loss(logits, targets, wt, seg, loss, dlog, wsl, stream), steps, warmup, stream)
+    if lwm.lwm_attn_check(wsl) != 0:
+        raise RuntimeError("device error in the packed loss")
+    nbytes = 2 * Bl * Sl * V * 2
+    out["packed_loss"] = {"shape": [Bl, Sl, V], "documents": sum(len(r) for r in w.lengths), "ms": ms,
+                          "bytes": nbytes,
+                          "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": hbm,
+                                       "unit": "GB/s", "frac": nbytes / (ms * 1e-3) / 1e9 / hbm}}
+    del logits, dlog, targets, wt, wsl
+    torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -394,12 +541,23 @@ def main():
                     help="backward path: dK/dV and dQ kernels (default) or one dK/dV/dQ kernel")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the packed workload and the RoPE / decode / packed-loss measurements")
+    ap.add_argument("--extras-only", action="store_true",
+                    help="run only the packed workload and the RoPE / decode / packed-loss measurements")
+    ap.add_argument("--extras-small", action="store_true",
+                    help="smaller extras (a 256K-token decode cache, a 16K-token packed-loss batch) for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank, world = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank)
+    elif args.extras_only:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        extras = run_extras(args, dev, torch.cuda.current_stream(), load_peaks(), None)
+        if rank == 0:
+            print(json.dumps(extras), flush=True)
     else:
         run_ours(args, rank, world)
     if world > 1:

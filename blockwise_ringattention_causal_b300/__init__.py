@@ -22,7 +22,9 @@ __all__ = [
     "LwmError", "library_path", "load_library",
     "lwm_attn_workspace_size", "lwm_attn_workspace_size_fwd", "lwm_attn_prepare", "lwm_attn_fwd", "lwm_attn_fwd_ring",
     "lwm_attn_fwd_prepared", "lwm_attn_bwd", "lwm_attn_bwd_prepared", "lwm_attn_bwd_stages",
-    "lwm_attn_check", "lwm_attn_set_wait_limit",
+    "lwm_attn_check", "lwm_attn_set_wait_limit", "lwm_attn_rope", "rope",
+    "lwm_attn_decode_workspace_size", "lwm_attn_decode", "decode",
+    "lwm_packed_loss_workspace_size", "lwm_packed_loss", "packed_loss",
     "lwm_status_string", "lwm_last_error", "new_workspace", "forward", "backward",
 ]
 
@@ -32,6 +34,7 @@ _LIB = None
 STATUS_NAMES = {
     0: "LWM_OK", 1: "LWM_ERR_INVALID_ARG", 2: "LWM_ERR_UNSUPPORTED", 3: "LWM_ERR_ALIGNMENT",
     4: "LWM_ERR_SEGMENTS", 5: "LWM_ERR_WORKSPACE", 6: "LWM_ERR_CUDA", 7: "LWM_ERR_TIMEOUT",
+    8: "LWM_ERR_LENGTHS", 9: "LWM_ERR_TARGETS",
 }
 
 # name -> (restype, argtypes)
@@ -50,7 +53,12 @@ _SIGNATURES = {
     "lwm_status_string": (ctypes.c_char_p, [_I]),
     "lwm_last_error": (ctypes.c_char_p, []),
     "lwm_attn_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
-    "lwm_attn_set_wait_limit": (_I, [_P, ctypes.c_uint64, _P]),
+    "lwm_attn_set_wait_limit": (_I, [ctypes.c_uint64]),
+    "lwm_attn_rope": (_I, [_P, _P, _P, ctypes.c_double, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "lwm_attn_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "lwm_attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lwm_packed_loss_workspace_size": (_Z, [_I, _I]),
+    "lwm_packed_loss": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _Z, _P]),
 }
 
 
@@ -233,10 +241,100 @@ def lwm_attn_bwd_stages(q, k, v, out, dout, lse, dq, dk, dv, stages, workspace, 
            "lwm_attn_bwd_stages")
 
 
-def lwm_attn_set_wait_limit(workspace, limit_ns, stream=None):
-    """Bound of the kernels' pipeline waits for calls with this workspace (0 = default 2 s)."""
-    _check(load_library().lwm_attn_set_wait_limit(_ptr(workspace), int(limit_ns), _stream(stream)),
-           "lwm_attn_set_wait_limit")
+def lwm_attn_rope(q, k, pos, theta, q_out, k_out, inverse=False, stream=None):
+    """RoPE rotation (or, with ``inverse``, its transpose) of q and/or k by ``pos``.
+
+    Either of (q, q_out) and (k, k_out) may be (None, None); out may be the input."""
+    ref = q if q is not None else k
+    B, S, H, D = _shape(ref)
+    for t, n in ((q, "q"), (k, "k"), (q_out, "q_out"), (k_out, "k_out")):
+        if t is not None:
+            _need(t, n, torch.bfloat16, (B, S, H, D))
+    if pos is not None:
+        _need(pos, "pos", torch.int32, (B, S))
+    _check(load_library().lwm_attn_rope(_ptr(q), _ptr(k), _ptr(pos), float(theta), _ptr(q_out), _ptr(k_out),
+                                        B, S, H, D, int(bool(inverse)), _stream(stream)), "lwm_attn_rope")
+
+
+def rope(q, k, pos, theta, inverse=False, stream=None):
+    """Rotated copies (q_rot, k_rot) of q and k (either may be None)."""
+    q_out = None if q is None else torch.empty_like(q)
+    k_out = None if k is None else torch.empty_like(k)
+    lwm_attn_rope(q, k, pos, theta, q_out, k_out, inverse, stream)
+    return q_out, k_out
+
+
+def lwm_attn_decode_workspace_size(B, T, S_max, H, D) -> int:
+    return int(load_library().lwm_attn_decode_workspace_size(B, T, S_max, H, D))
+
+
+def lwm_attn_decode(q, k_cache, v_cache, kv_len, out, lse, workspace, stream=None):
+    """Attention of the T newest tokens (q [B, T, H, D]) against the caches [B, S_max, H, D]."""
+    B, T, H, D = _shape(q)
+    S_max = int(k_cache.shape[1])
+    _need(q, "q", torch.bfloat16)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16, (B, S_max, H, D))
+    _need(out, "out", torch.bfloat16, (B, T, H, D))
+    _need(lse, "lse", torch.float32, (B, H, T))
+    if kv_len is not None:
+        _need(kv_len, "kv_len", torch.int32, (B,))
+    _check(load_library().lwm_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), _ptr(out), _ptr(lse),
+                                          B, T, S_max, H, D, _ptr(workspace), workspace.numel(), _stream(stream)),
+           "lwm_attn_decode")
+
+
+def decode(q, k_cache, v_cache, kv_len=None, workspace=None, stream=None):
+    """Allocate out/lse (and a workspace if none is given) and decode. Returns (out, lse, workspace)."""
+    B, T, H, D = _shape(q)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = lwm_attn_decode_workspace_size(B, T, int(k_cache.shape[1]), H, D)
+        if n == 0:
+            raise ValueError("unsupported decode sizes")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    lwm_attn_decode(q, k_cache, v_cache, kv_len, out, lse, workspace, stream)
+    return out, lse, workspace
+
+
+def lwm_packed_loss_workspace_size(B, S) -> int:
+    return int(load_library().lwm_packed_loss_workspace_size(B, S))
+
+
+def lwm_packed_loss(logits, targets, weight, seg_ids, loss, dlogits, workspace, stream=None):
+    """Re-weighted packed cross-entropy: loss (float64 [1]) and, if given, dlogits."""
+    if logits.dim() != 3:
+        raise ValueError("logits must be [B, S, V]")
+    B, S, V = (int(x) for x in logits.shape)
+    _need(logits, "logits", torch.bfloat16)
+    _need(targets, "targets", torch.int32, (B, S))
+    if weight is not None:
+        _need(weight, "weight", torch.float32, (B, S))
+    if seg_ids is not None:
+        _need(seg_ids, "seg_ids", torch.int32, (B, S))
+    _need(loss, "loss", torch.float64)
+    if dlogits is not None:
+        _need(dlogits, "dlogits", torch.bfloat16, (B, S, V))
+    _check(load_library().lwm_packed_loss(_ptr(logits), _ptr(targets), _ptr(weight), _ptr(seg_ids), _ptr(loss),
+                                          _ptr(dlogits), B, S, V, _ptr(workspace), workspace.numel(),
+                                          _stream(stream)), "lwm_packed_loss")
+
+
+def packed_loss(logits, targets, weight=None, seg_ids=None, grad=True, workspace=None, stream=None):
+    """Allocate the outputs and run lwm_packed_loss. Returns (loss [1] float64, dlogits or None, workspace)."""
+    B, S, V = (int(x) for x in logits.shape)
+    loss = torch.empty(1, dtype=torch.float64, device=logits.device)
+    dlogits = torch.empty_like(logits) if grad else None
+    if workspace is None:
+        workspace = torch.zeros(lwm_packed_loss_workspace_size(B, S), dtype=torch.uint8, device=logits.device)
+    lwm_packed_loss(logits, targets, weight, seg_ids, loss, dlogits, workspace, stream)
+    return loss, dlogits, workspace
+
+
+def lwm_attn_set_wait_limit(limit_ns):
+    """Bound of the kernels' pipeline waits for every later launch of this process (0 = 2 s)."""
+    _check(load_library().lwm_attn_set_wait_limit(int(limit_ns)), "lwm_attn_set_wait_limit")
 
 
 def lwm_attn_check(workspace, stream=None) -> int:

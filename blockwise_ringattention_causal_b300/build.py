@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "liblwm_attn.so")
-SOURCES = ["api.cu", "meta.cu", "fwd.cu", "bwd.cu", "bwd_fused.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "meta.cu", "fwd.cu", "bwd.cu", "bwd_fused.cu", "rope.cu", "decode.cu", "loss.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

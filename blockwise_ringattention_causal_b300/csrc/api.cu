@@ -1,7 +1,9 @@
 // C ABI of the attention library: argument checks, TMA tensor maps and kernel
 // launches. See include/lwm_attn.h for the contract of every entry point.
+#include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -21,6 +23,7 @@ struct DeviceInfo {
 };
 
 std::mutex g_mu;
+std::atomic<uint64_t> g_wait_limit_ns{0};   // lwm_attn_set_wait_limit (0 = WAIT_LIMIT_NS)
 DeviceInfo g_dev[MAX_DEVICES];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -125,6 +128,14 @@ lwm_status check_sizes(int B, int S, int H, int D) {
   return LWM_OK;
 }
 
+WaitBound wait_bound() {
+  const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  WaitBound b;
+  b.limit_ns = v ? v : WAIT_LIMIT_NS;
+  b.test = b.limit_ns < SHORT_WAIT_LIMIT_NS ? 1 : 0;
+  return b;
+}
+
 lwm_status check_device() {
   DeviceInfo d;
   return device_info(d);
@@ -166,8 +177,6 @@ lwm_status fwd_common(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, l
   Problem p{B, S, H, d.num_sms};
   return from_cuda(launch_fwd(tq, tk, tv, out, lse, p, ws, stream));
 }
-
-__global__ void set_u64_kernel(unsigned long long *p, unsigned long long v) { *p = v; }
 
 lwm_status check_fwd_args(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_bf16 *v, lwm_bf16 *out, float *lse,
                           int B, int S, int H, int D, void *ws, size_t ws_bytes) {
@@ -355,16 +364,76 @@ lwm_status lwm_attn_check(void *workspace, lwm_stream stream) {
   LWM_TRY(from_cuda(cudaMemcpy(&word, hdr + HDR_ERR, sizeof(int), cudaMemcpyDeviceToHost)));
   if (word != 0) LWM_TRY(from_cuda(cudaMemset(hdr + HDR_ERR, 0, sizeof(int))));
   if (word & ERRBIT_SEGMENTS) return LWM_ERR_SEGMENTS;
+  if (word & ERRBIT_LENGTHS) return LWM_ERR_LENGTHS;
+  if (word & ERRBIT_TARGETS) return LWM_ERR_TARGETS;
   if (word & ERRBIT_TIMEOUT) return LWM_ERR_TIMEOUT;
   return LWM_OK;
 }
 
-lwm_status lwm_attn_set_wait_limit(void *workspace, uint64_t limit_ns, lwm_stream stream) {
-  if (!workspace) return LWM_ERR_INVALID_ARG;
+lwm_status lwm_attn_rope(const lwm_bf16 *q, const lwm_bf16 *k, const int32_t *pos, double theta, lwm_bf16 *q_out,
+                         lwm_bf16 *k_out, int B, int S, int H, int D, int inverse, lwm_stream stream) {
+  LWM_TRY(check_sizes(B, S, H, D));
+  if (!(theta > 0.0) || !std::isfinite(theta) || (inverse != 0 && inverse != 1)) return LWM_ERR_INVALID_ARG;
+  if ((q == nullptr) != (q_out == nullptr) || (k == nullptr) != (k_out == nullptr) || (!q && !k))
+    return LWM_ERR_INVALID_ARG;
+  if ((q && (!aligned16(q) || !aligned16(q_out))) || (k && (!aligned16(k) || !aligned16(k_out))) ||
+      (pos && !aligned4(pos)))
+    return LWM_ERR_ALIGNMENT;
+  DeviceInfo d;
+  LWM_TRY(device_info(d));
+  return from_cuda(launch_rope(q, k, pos, theta, q_out, k_out, B, S, H, inverse != 0, d.num_sms, stream));
+}
+
+size_t lwm_attn_decode_workspace_size(int B, int T, int S_max, int H, int D) {
+  if (B <= 0 || B > 65535 || T < 1 || T > 4 || S_max < T || H <= 0 || D != HD) return 0;
+  if (static_cast<long long>(B) * S_max * H >= (1ll << 31)) return 0;
+  return decode_layout(B, T, S_max, H).total;
+}
+
+lwm_status lwm_attn_decode(const lwm_bf16 *q, const lwm_bf16 *k_cache, const lwm_bf16 *v_cache,
+                           const int32_t *kv_len, lwm_bf16 *out, float *lse, int B, int T, int S_max, int H, int D,
+                           void *workspace, size_t workspace_bytes, lwm_stream stream) {
+  if (B <= 0 || T <= 0 || S_max <= 0 || H <= 0 || D <= 0) return LWM_ERR_INVALID_ARG;
+  if (D != HD || T > 4) return LWM_ERR_UNSUPPORTED;
+  const size_t need = lwm_attn_decode_workspace_size(B, T, S_max, H, D);
+  if (need == 0) return LWM_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !out || !lse || !workspace) return LWM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned4(lse) ||
+      (kv_len && !aligned4(kv_len)))
+    return LWM_ERR_ALIGNMENT;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LWM_ERR_WORKSPACE;
-  auto *word = reinterpret_cast<unsigned long long *>(static_cast<int *>(workspace) + HDR_WAIT_LIMIT);
-  set_u64_kernel<<<1, 1, 0, stream>>>(word, static_cast<unsigned long long>(limit_ns));
-  return from_cuda(cudaGetLastError());
+  if (workspace_bytes < need) return LWM_ERR_INVALID_ARG;
+  DeviceInfo d;
+  LWM_TRY(device_info(d));
+  return from_cuda(launch_decode(q, k_cache, v_cache, kv_len, out, lse, B, T, S_max, H, workspace, stream));
+}
+
+size_t lwm_packed_loss_workspace_size(int B, int S) {
+  if (B <= 0 || S <= 0 || B > 65535 || static_cast<long long>(B) * S >= (1ll << 31)) return 0;
+  return loss_layout(B, S).total;
+}
+
+lwm_status lwm_packed_loss(const lwm_bf16 *logits, const int32_t *targets, const float *weight,
+                           const int32_t *seg_ids, double *loss, lwm_bf16 *dlogits, int B, int S, int V,
+                           void *workspace, size_t workspace_bytes, lwm_stream stream) {
+  if (B <= 0 || S <= 0 || V <= 0) return LWM_ERR_INVALID_ARG;
+  const size_t need = lwm_packed_loss_workspace_size(B, S);
+  if (need == 0) return LWM_ERR_INVALID_ARG;
+  if (V % 8 != 0) return LWM_ERR_UNSUPPORTED;
+  if (!logits || !targets || !loss || !workspace) return LWM_ERR_INVALID_ARG;
+  if (!aligned16(logits) || (dlogits && !aligned16(dlogits)) || !aligned4(targets) || (weight && !aligned4(weight)) ||
+      (seg_ids && !aligned4(seg_ids)) || (reinterpret_cast<uintptr_t>(loss) & 7u) != 0)
+    return LWM_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LWM_ERR_WORKSPACE;
+  if (workspace_bytes < need) return LWM_ERR_INVALID_ARG;
+  DeviceInfo d;
+  LWM_TRY(device_info(d));
+  return from_cuda(launch_packed_loss(logits, targets, weight, seg_ids, loss, dlogits, B, S, V, workspace, stream));
+}
+
+lwm_status lwm_attn_set_wait_limit(uint64_t limit_ns) {
+  g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+  return LWM_OK;
 }
 
 const char *lwm_last_error(void) { return g_last_error; }
@@ -379,6 +448,8 @@ const char *lwm_status_string(lwm_status status) {
     case LWM_ERR_WORKSPACE: return "LWM_ERR_WORKSPACE: workspace must be 256-byte aligned";
     case LWM_ERR_CUDA: return "LWM_ERR_CUDA: a CUDA call failed";
     case LWM_ERR_TIMEOUT: return "LWM_ERR_TIMEOUT: a device pipeline wait exceeded its bound";
+    case LWM_ERR_LENGTHS: return "LWM_ERR_LENGTHS: a decode kv_len is outside [T, S_max]";
+    case LWM_ERR_TARGETS: return "LWM_ERR_TARGETS: a weighted token's target is outside [0, V)";
   }
   return "unknown lwm_status";
 }

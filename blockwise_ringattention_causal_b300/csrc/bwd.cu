@@ -110,6 +110,7 @@ constexpr int BW_THREADS = BW_WARPS * 32;
 constexpr int BW_PRODUCER = 8;
 constexpr int BW_MMA = 9;       // MMA issuer (owns TMEM)
 constexpr int BW_MMA2 = 10;     // second MMA issuer
+constexpr int BW_MMA3 = 11;     // third MMA issuer (dQ kernel: the S products)
 constexpr int RT_BYTES = BM * 4;   // 128 row terms (int32 / fp32)
 
 __device__ __forceinline__ void load_tile(const CUtensorMap *m, uint64_t *bar, uint8_t *dst, int h, int row0, int b) {
@@ -152,6 +153,7 @@ struct BwArgs {
   int B, S, H, nT, S_pad, n_list, n_items;
   float scale_log2;   // log2(e) / sqrt(D)
   float inv_sqrt_d;
+  WaitBound wait;
 };
 
 struct BwItem {
@@ -193,7 +195,11 @@ __device__ __forceinline__ int range_tiles(const TileRange &R) { return R.empty(
 // (bf16 pairs) | dV [256, 384) | dK [384, 512). The softmax warps read X out first
 // thing in each phase, so the next S^T or dP^T runs while they still work on this one;
 // P^T and dS^T wait in columns of their own for their dV / dK products. Two MMA issuers:
-// warp 9 the X products (S^T, dP^T, alternating), warp 10 the accumulating ones.
+// warp 9 the X products (S^T, dP^T, alternating), warp 10 the accumulating ones. Warp 11
+// idles. (Measured slower, interleaved A/B: a third issuer for the dK products, 1.7 %,
+// since they then interleave with the next S^T on the tensor core and delay it; and
+// splitting every X product into two 64-query halves, one chain per softmax warpgroup,
+// 13 %.)
 constexpr int KV_STAGE_BYTES = 2 * TILE_BYTES + 3 * RT_BYTES;   // Q, dO, lo, lse2, delta
 constexpr int KV_STAGE_STRIDE = (KV_STAGE_BYTES + 1023) & ~1023;
 constexpr int KVB_SM_K = 0, KVB_SM_V = TILE_BYTES, KVB_SM_ST = 2 * TILE_BYTES;
@@ -208,7 +214,7 @@ struct KvbBars {
   uint64_t pt_free, ds_free;          // dV / dK product done with PT / DS
   uint64_t acc_full, acc_empty;
   uint64_t item_full[2], item_empty[2];
-  uint64_t drain;
+  uint64_t drain, never;
   int item[2];
   uint32_t tmem_base;
   WaitCtl ctl;
@@ -253,6 +259,7 @@ __device__ __forceinline__ bool kv_producer(const CUtensorMap *tq, const CUtenso
       ++fill;
     }
     if (!ok) break;
+    if (a.wait.test && it == 0 && !(ok = test_expiry_wait(&bars->never, abort))) break;
   }
   bars->fill = fill;
   bars->own_issued = own;
@@ -548,8 +555,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 2);
-    bars->ctl.abort = 0;
-    bars->ctl.limit_ns = pipeline_wait_limit(a.hdr);
+    mbar_init(&bars->never, 1);
+    bars->ctl.init(a.wait);
     bars->fill = bars->use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
   }
@@ -617,9 +624,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 //   S    = Q . K_j^T  -> A_{j % 2}      dP = dO . V_j^T -> B
 //   P    = exp2(S c - lse2) (masked),  dS = P (dP - delta)  -> bf16 over A_{j % 2}
 //   dQ  += dS . K_j   (C; scaled by 1/sqrt(D) in the epilogue)
-// TMEM: A0 [0, 128), A1 [128, 256), B [256, 384), C [384, 512). Two MMA issuers: warp
-// 9 runs S(j) (two tiles ahead) and dQ(j), warp 10 runs dP(j). Deterministic: every dQ
-// row is summed by one CTA in a fixed order.
+// TMEM: A0 [0, 128), A1 [128, 256), B [256, 384), C [384, 512). Three MMA issuers: warp
+// 9 runs dQ(j), warp 10 dP(j), warp 11 S(j) (up to two tiles ahead). Deterministic: every
+// dQ row is summed by one CTA in a fixed order.
 constexpr int DQ_KSTAGES = 3, DQ_VSTAGES = 2;
 constexpr int DQ_SM_Q = 0, DQ_SM_DO = TILE_BYTES, DQ_SM_K = 2 * TILE_BYTES;
 constexpr int DQ_SM_V = DQ_SM_K + DQ_KSTAGES * TILE_BYTES;
@@ -634,9 +641,10 @@ struct DqBars {
   // softmax cannot complete a second phase of that slot's barrier before the wait (a
   // single barrier could run two phases ahead and alias the parity).
   uint64_t s_full[2], dp_full, ds_full[2], ds_dp;
+  uint64_t a_free[2];   // dQ(j) has completed: slot A_{j % 2} may take S(j + 2)
   uint64_t acc_full, acc_empty;
   uint64_t item_full[2], item_empty[2];
-  uint64_t drain;
+  uint64_t drain, never;
   int item[2];
   uint32_t tmem_base;
   WaitCtl ctl;
@@ -681,6 +689,9 @@ __device__ __forceinline__ bool dq_producer(const CUtensorMap *tq, const CUtenso
       ++v_fill;
     }
     if (!ok) break;
+    // failure test only: wait, with this item's copies and products in flight, for a
+    // phase that never completes (the short test bound makes the wait run out)
+    if (a.wait.test && it == 0 && !(ok = test_expiry_wait(&bars->never, abort))) break;
   }
   bars->k_fill = k_fill;
   bars->v_fill = v_fill;
@@ -688,16 +699,20 @@ __device__ __forceinline__ bool dq_producer(const CUtensorMap *tq, const CUtenso
   return ok;
 }
 
-// MMA chains of the dQ kernel. chain 0 (warp 9): S(j) = Q K_j^T into A_{j % 2} (two
-// ahead), dQ += dS(j) K_j once the softmax has written dS(j); chain 1 (warp 10): dP(j) =
-// dO V_j^T into B, each after the softmax has finished reading the previous dP.
+// MMA chains of the dQ kernel, one issuing warp each:
+//   chain 0 (warp 9):  dQ += dS(j) K_j once the softmax has written dS(j) over A_{j % 2};
+//                      then releases K_j and the slot A_{j % 2} (a_free, on completion);
+//   chain 1 (warp 10): dP(j) = dO V_j^T into B, after the softmax read the previous dP;
+//   chain 2 (warp 11): S(j) = Q K_j^T into A_{j % 2}, once the dQ product that last read
+//                      that slot has completed (it runs up to two tiles ahead).
 __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *bars, uint32_t tmem, int chain,
                                        int lane) {
   WaitCtl *abort = &bars->ctl;
   const uint32_t q_s = smem_u32(smem + DQ_SM_Q), do_s = smem_u32(smem + DQ_SM_DO);
   const uint32_t k0_s = smem_u32(smem + DQ_SM_K), v0_s = smem_u32(smem + DQ_SM_V);
   int k_use = 0, v_use = 0, own = 0, dp_issued = 0;
-  int k_seen = 0;   // K stages whose arrival chain 0 has observed (the abort path waits for the rest)
+  int k_seen = 0;               // K stages whose arrival chain 2 has observed (the abort path waits for the rest)
+  int a_uses[2] = {0, 0};       // S products written into each A slot so far (chain 2)
   uint32_t dsf_par[2] = {0, 0}, dsp_par = 0, ae_par = 1;
   bool ok = true;
   for (int it = 0; ok; ++it) {
@@ -709,24 +724,14 @@ __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *b
     if (item < 0) break;
     const BwItem I = bw_decode(a, item);
     const int n = range_tiles(dq_range(a, I));
-    if (!(ok = mbar_wait(&bars->own_full, it & 1, abort))) break;
-    ++own;
-    tc_fence_after();
+    if (chain != 0) {   // Q (S products) and dO (dP products) resident
+      if (!(ok = mbar_wait(&bars->own_full, it & 1, abort))) break;
+      ++own;
+    }
+    const int kb = k_use;
+    auto k_stage = [&](int j) { return (kb + j) % DQ_KSTAGES; };
+    auto k_par = [&](int j) { return uint32_t((kb + j) / DQ_KSTAGES) & 1u; };
     if (chain == 0) {
-      const int kb = k_use;
-      auto k_s = [&](int j) { return k0_s + uint32_t((kb + j) % DQ_KSTAGES) * TILE_BYTES; };
-      auto issue_s = [&](int j) -> bool {   // S(j) = Q K_j^T into A_{j % 2}
-        if (!mbar_wait(&bars->k_full[(kb + j) % DQ_KSTAGES], ((kb + j) / DQ_KSTAGES) & 1, abort)) return false;
-        k_seen = kb + j + 1;
-        tc_fence_after();
-        if (lane == 0) {
-          mma_tile_kk(tmem + uint32_t(j & 1) * 128, q_s, k_s(j), false);
-          mma_commit(&bars->s_full[j & 1]);
-        }
-        __syncwarp();
-        return true;
-      };
-      if (n > 0) ok = issue_s(0) && (n < 2 || issue_s(1));
       for (int j = 0; j < n && ok; ++j) {
         if (!(ok = mbar_wait(&bars->ds_full[j & 1], dsf_par[j & 1], abort))) break;
         dsf_par[j & 1] ^= 1;
@@ -734,17 +739,35 @@ __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *b
           if (!(ok = mbar_wait(&bars->acc_empty, ae_par, abort))) break;
           ae_par ^= 1;
         }
+        // K_j arrived (chain 2 saw it before S(j)); the stage stays until this chain releases it
+        if (!(ok = mbar_wait(&bars->k_full[k_stage(j)], k_par(j), abort))) break;
         tc_fence_after();
         if (lane == 0) {
-          mma_tile_ts(tmem + DQ_COL_C, tmem + uint32_t(j & 1) * 128, k_s(j), j > 0);   // dQ += dS K
-          mma_commit(&bars->k_empty[(kb + j) % DQ_KSTAGES]);
+          mma_tile_ts(tmem + DQ_COL_C, tmem + uint32_t(j & 1) * 128,
+                      k0_s + uint32_t(k_stage(j)) * TILE_BYTES, j > 0);   // dQ += dS K
+          mma_commit(&bars->k_empty[k_stage(j)]);
+          mma_commit(&bars->a_free[j & 1]);
         }
         __syncwarp();
-        if (j + 2 < n && !(ok = issue_s(j + 2))) break;   // A_{j % 2} is reused after dQ(j), in order
       }
       if (!ok) break;
-      k_use = kb + n;
       if (lane == 0 && n > 0) mma_commit(&bars->acc_full);
+      __syncwarp();
+    } else if (chain == 2) {
+      for (int j = 0; j < n && ok; ++j) {
+        if (!(ok = mbar_wait(&bars->k_full[k_stage(j)], k_par(j), abort))) break;
+        k_seen = kb + j + 1;
+        const int s = j & 1;
+        if (a_uses[s] > 0 && !(ok = mbar_wait(&bars->a_free[s], uint32_t(a_uses[s] - 1) & 1u, abort))) break;
+        ++a_uses[s];
+        tc_fence_after();
+        if (lane == 0) {
+          mma_tile_kk(tmem + uint32_t(s) * 128, q_s, k0_s + uint32_t(k_stage(j)) * TILE_BYTES, false);   // S = Q K^T
+          mma_commit(&bars->s_full[s]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
     } else {
       for (int j = 0; j < n && ok; ++j, ++v_use) {
         const int vs = v_use % DQ_VSTAGES;
@@ -764,10 +787,13 @@ __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *b
       }
       if (!ok) break;
     }
-    if (lane == 0) mma_commit(&bars->own_empty);
-    __syncwarp();
+    k_use = kb + n;
+    if (chain != 0) {
+      if (lane == 0) mma_commit(&bars->own_empty);
+      __syncwarp();
+    }
   }
-  if (lane == 0 && chain == 0) {
+  if (lane == 0 && chain == 2) {
     bars->k_use = k_seen;
     bars->own_used = own;
   }
@@ -906,8 +932,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->ds_full[s], 8);
+      mbar_init(&bars->a_free[s], 1);
       mbar_init(&bars->item_full[s], 1);
-      mbar_init(&bars->item_empty[s], 10);  // softmax 8 + MMA 2 warps
+      mbar_init(&bars->item_empty[s], 11);  // softmax 8 + MMA 3 warps
     }
     mbar_init(&bars->own_full, 1);
     mbar_init(&bars->own_empty, 2);
@@ -915,9 +942,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     mbar_init(&bars->ds_dp, 8);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
-    mbar_init(&bars->drain, 2);
-    bars->ctl.abort = 0;
-    bars->ctl.limit_ns = pipeline_wait_limit(a.hdr);
+    mbar_init(&bars->drain, 3);
+    mbar_init(&bars->never, 1);
+    bars->ctl.init(a.wait);
     bars->k_fill = bars->k_use = bars->v_fill = bars->v_use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
   }
@@ -941,7 +968,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   } else if (warp == BW_PRODUCER) {
     if (lane == 0) ok = dq_producer(&tq, &tk, &tv, &tdo, a, smem, bars);
     __syncwarp();
-  } else if (warp == BW_MMA || warp == BW_MMA2) {
+  } else if (warp == BW_MMA || warp == BW_MMA2 || warp == BW_MMA3) {
     ok = dq_mma(a, smem, bars, tmem, warp - BW_MMA, lane);
   }
 
@@ -959,7 +986,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         bounded_wait_plain(&bars->v_full[k % DQ_VSTAGES], (k / DQ_VSTAGES) & 1);
       if (bars->own_issued > bars->own_used) bounded_wait_plain(&bars->own_full, (bars->own_issued - 1) & 1);
     }
-    if ((warp == BW_MMA || warp == BW_MMA2) && lane == 0) {
+    if ((warp == BW_MMA || warp == BW_MMA2 || warp == BW_MMA3) && lane == 0) {
       mma_commit(&bars->drain);
       bounded_wait_plain(&bars->drain, 0);
     }
@@ -999,6 +1026,7 @@ BwArgs bw_args(const Problem &p, void *workspace, const int *list) {
   a.n_items = a.n_list * p.H;
   a.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
   a.inv_sqrt_d = 1.f / sqrtf(float(HD));
+  a.wait = wait_bound();
   return a;
 }
 

@@ -71,7 +71,7 @@ struct FbBars {
   uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty;
   uint64_t acc_full, acc_empty;
   uint64_t item_full[2], item_empty[2];
-  uint64_t drain;
+  uint64_t drain, never;
   int item[2];
   uint32_t tmem_base;
   WaitCtl ctl;
@@ -91,6 +91,7 @@ struct FbArgs {
   int B, S, H, nT, S_pad, n_list, n_items;
   float scale_log2;    // log2(e) / sqrt(D)
   float inv_sqrt_d;
+  WaitBound wait;
 };
 
 struct FbItem {
@@ -214,6 +215,9 @@ __device__ __forceinline__ bool fb_producer(const CUtensorMap *tq, const CUtenso
       ++do_fill;
     }
     if (!ok) break;
+    // failure test only: wait, with this item's copies and products in flight, for a
+    // phase that never completes (the short test bound makes the wait run out)
+    if (a.wait.test && it == 0 && !(ok = test_expiry_wait(&bars->never, abort))) break;
   }
   bars->q_fill = q_fill;
   bars->do_fill = do_fill;
@@ -570,8 +574,8 @@ __global__ void __launch_bounds__(FB_THREADS, 1)
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 1);
-    bars->ctl.abort = 0;
-    bars->ctl.limit_ns = pipeline_wait_limit(a.hdr);
+    mbar_init(&bars->never, 1);
+    bars->ctl.init(a.wait);
     bars->q_fill = bars->q_use = bars->do_fill = bars->do_use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
   }
@@ -656,6 +660,7 @@ cudaError_t launch_dkdvq(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   a.n_items = a.n_list * p.H;
   a.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
   a.inv_sqrt_d = 1.f / sqrtf(float(HD));
+  a.wait = wait_bound();
   float *dqacc = reinterpret_cast<float *>(base + w.off_dqacc);
   cudaError_t e = cudaMemsetAsync(dqacc, 0, w.dqacc_bytes, stream);
   if (e != cudaSuccess) return e;

@@ -25,13 +25,14 @@ constexpr int NBINS = 4096;                    // cost buckets of the longest-fi
 // Device error word values (a bit mask; lwm_attn_check maps it to a status).
 constexpr int ERRBIT_SEGMENTS = 1;
 constexpr int ERRBIT_TIMEOUT = 2;
+constexpr int ERRBIT_LENGTHS = 4;   // decode: a kv_len outside [T, S_max]
+constexpr int ERRBIT_TARGETS = 8;   // packed loss: a weighted token's target outside [0, V)
 
 // ----------------------------------------------------------------------------- workspace
 // Header words (int32) at the start of the workspace.
 enum HeaderWord {
   HDR_ERR = 0,          // error bits
   HDR_KV_CHUNK = 1,     // ring chunk length in key tiles
-  HDR_WAIT_LIMIT = 2,   // words 2-3: bound of the pipeline waits in ns (uint64; 0 = WAIT_LIMIT_NS)
   HDR_TICKET_FWD = 4,   // persistent-scheduler tickets and exit counters
   HDR_DONE_FWD = 5,
   HDR_TICKET_DKDV = 6,
@@ -156,32 +157,58 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // time (a phase that never completes would otherwise hang the GPU) or as soon as
 // another role of the CTA has raised `abort` after its own wait gave up. The kernels
 // then let copies and products in flight land, free TMEM and return; the host reads
-// the error word. limit_ns comes from the workspace header (HDR_WAIT_LIMIT, 0 = the
-// default below), so a test can shorten it and watch the waits run out.
+// the error word. The bound is a launch parameter (WaitBound, from the process-wide
+// setting of lwm_attn_set_wait_limit), so that a test can shorten it and watch the
+// waits run out; the fast path of a wait is a single try_wait on the barrier.
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s: far above any legitimate wait
+
+// Bounds below this are test settings (the failure test): a wait whose first try_wait
+// fails then reads the clock on every poll, and each kernel's producer waits once, with
+// work in flight, for a phase that never completes (test_expiry_wait), so that the bound
+// runs out for certain. A suspending try_wait usually sees a real phase complete before
+// any clock check, so shortening the bound alone would not make waits run out.
+constexpr uint64_t SHORT_WAIT_LIMIT_NS = 1000000ull;
+
+// The bound as a kernel launch parameter.
+struct WaitBound {
+  unsigned long long limit_ns;   // WAIT_LIMIT_NS unless a test shortened it
+  int test;                      // limit_ns < SHORT_WAIT_LIMIT_NS: the failure test
+};
 
 struct WaitCtl {
   int abort;           // raised by the role whose wait ran out; the others poll it
   int unused;
   uint64_t limit_ns;   // bound of the pipeline waits
+
+  __device__ __forceinline__ void init(const WaitBound &b) {
+    abort = 0;
+    limit_ns = b.limit_ns;
+  }
 };
 
-__device__ __forceinline__ uint64_t pipeline_wait_limit(const int *hdr) {
-  const uint64_t v = *reinterpret_cast<const uint64_t *>(hdr + HDR_WAIT_LIMIT);
-  return v ? v : WAIT_LIMIT_NS;
-}
-
+// The fast path is one (suspending) try_wait; only after it fails are the abort flag and
+// the clock consulted: every 64 polls, or on every poll under a test bound.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, WaitCtl *ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   const uint64_t limit = ctl->limit_ns;
+  const uint32_t check = limit < SHORT_WAIT_LIMIT_NS ? 0u : 63u;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
+    if ((it & check) == 0u) {
       if (*reinterpret_cast<volatile int *>(&ctl->abort)) return false;
       if (global_timer_ns() - t0 > limit) return false;
     }
   }
+}
+
+// The failure test's wait: a phase that nothing ever completes (an mbarrier that no
+// thread arrives on), waited for under the test's short bound, at a point where copies
+// and products are in flight, so that the abort path has real work to let land.
+// Out of line: it sits on the producers' cold path only, and inlining it would change
+// the register allocation of the whole kernel.
+static __device__ __noinline__ bool test_expiry_wait(uint64_t *never, WaitCtl *ctl) {
+  return mbar_wait(never, 0, ctl);
 }
 
 // Spins (bounded like mbar_wait) until *count reaches target.

@@ -46,7 +46,7 @@ struct FwdBars {
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_free, p_full[2], pv_done[2], o_empty[2];
   uint64_t item_full[2], item_empty[2];
-  uint64_t drain;
+  uint64_t drain, never;
   int item[2];
   uint32_t tmem_base;
   WaitCtl ctl;
@@ -71,6 +71,7 @@ struct FwdArgs {
   float *lse;
   int B, S, H, nP, n_list, n_items, S_pad;
   float scale_log2;   // log2(e) / sqrt(D)
+  WaitBound wait;
 };
 
 struct Item {
@@ -166,6 +167,9 @@ __device__ bool producer_role(const CUtensorMap *tq, const CUtensorMap *tk, cons
       }
     }
     if (!ok) break;
+    // failure test only: wait, with this item's copies and products in flight, for a
+    // phase that never completes (the short test bound makes the wait run out)
+    if (a.wait.test && it == 0 && !(ok = test_expiry_wait(&bars->never, abort))) break;
   }
   bars->kv_fill = kv_fill;
   bars->q_issued = q_issued;
@@ -485,8 +489,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       mbar_init(&bars->item_empty[t], 11);   // softmax 8 + MMA 3 warps
     }
     mbar_init(&bars->drain, 3);
-    bars->ctl.abort = 0;
-    bars->ctl.limit_ns = pipeline_wait_limit(a.hdr);
+    mbar_init(&bars->never, 1);
+    bars->ctl.init(a.wait);
     bars->kv_fill = bars->kv_use_k = bars->kv_use_v[0] = bars->kv_use_v[1] = bars->q_issued = bars->q_used = 0;
     bars->s_issued[0] = bars->s_issued[1] = 0;
     fence_mbar_init();
@@ -579,6 +583,7 @@ cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   a.n_list = p.B * w.nP;
   a.n_items = a.n_list * p.H;
   a.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
+  a.wait = wait_bound();
   const int grid = a.n_items < p.num_sms ? a.n_items : p.num_sms;
   fwd_kernel<<<grid, FWD_THREADS, FWD_SMEM, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();

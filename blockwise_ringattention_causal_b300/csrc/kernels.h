@@ -51,11 +51,45 @@ cudaError_t launch_dq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtens
                       const CUtensorMap &tdo, void *dq, const Problem &p, void *workspace,
                       cudaStream_t stream);
 
+// RoPE rotation of q and/or k (either may be null), in place when y == x.
+cudaError_t launch_rope(const void *x0, const void *x1, const int *pos, double theta, void *y0, void *y1, int B,
+                        int S, int H, bool inverse, int num_sms, cudaStream_t stream);
+
+// Decoding against a key/value cache: workspace layout (header words, then the
+// per-split (m, l) pairs and unnormalised outputs) and the two launches (splits, merge).
+struct DecodeLayout {
+  int split_len, n_split;
+  size_t off_ml, off_o, total;
+};
+DecodeLayout decode_layout(int B, int T, int S_max, int H);
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const int *kv_len, void *out, float *lse,
+                          int B, int T, int S_max, int H, void *workspace, cudaStream_t stream);
+
+// Document starts lo[b, i] (the first pass of the metadata pre-pass, from seg alone);
+// blk_last holds B * ceil(S_pad / 1024) ints of carries.
+cudaError_t launch_doc_starts(const int *seg, int B, int S, int S_pad, int *lo, int *blk_last, int *err,
+                              cudaStream_t stream);
+
+// Packed-loss re-weighting: workspace layout and the launches.
+struct LossLayout {
+  int S_pad, n_blk, n_cta;
+  size_t off_lo, off_blk, off_docsum, off_part, total;
+};
+LossLayout loss_layout(int B, int S);
+cudaError_t launch_packed_loss(const void *logits, const int *targets, const float *weight, const int *seg,
+                               double *loss, void *dlogits, int B, int S, int V, void *workspace,
+                               cudaStream_t stream);
+
 }  // namespace lwm
 
 #include "lwm_attn.h"
 
 namespace lwm {
+
+// The bound of the kernels' pipeline waits for the next launches (process-wide,
+// lwm_attn_set_wait_limit; WAIT_LIMIT_NS unless a test shortened it). api.cu.
+struct WaitBound;
+WaitBound wait_bound();
 
 // Host-side argument checks shared by the entry points (api.cu).
 lwm_status check_sizes(int B, int S, int H, int D);

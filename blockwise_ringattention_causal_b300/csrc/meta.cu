@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(META_THREADS) meta_sort_kernel(const int *__re
       const int *lr = lo + size_t(b) * S_pad;
       return range_size(lr, S, (2 * p) * BM) + range_size(lr, S, (2 * p + 1) * BM);
     } else if (which == 1) {
-      const int b = idx / nT, kt = idx % nT;
+      const int kt = idx % nT;
       const int k0 = kt * BN, e = kend[idx];
       return e > k0 ? (e - 1) / BM - k0 / BM + 1 : 0;
     } else {
@@ -231,6 +231,14 @@ __global__ void __launch_bounds__(META_THREADS) meta_sort_kernel(const int *__re
 }
 
 }  // namespace
+
+cudaError_t launch_doc_starts(const int *seg, int B, int S, int S_pad, int *lo, int *blk_last, int *err,
+                              cudaStream_t stream) {
+  const dim3 g1((S_pad + META_THREADS - 1) / META_THREADS, B);
+  meta_lo_kernel<<<g1, META_THREADS, 0, stream>>>(seg, nullptr, S, S_pad, lo, blk_last, err);
+  meta_lo_carry_kernel<<<g1, META_THREADS, 0, stream>>>(seg, S, S_pad, lo, blk_last);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_meta(const int *seg, const int *pos, int B, int S, int kv_chunk, void *workspace,
                         cudaStream_t stream) {

@@ -68,7 +68,9 @@ typedef enum {
   LWM_ERR_SEGMENTS = 4,     /* device: seg_ids / pos break the preconditions above */
   LWM_ERR_WORKSPACE = 5,    /* workspace not 256-byte aligned */
   LWM_ERR_CUDA = 6,         /* a CUDA runtime or driver call failed */
-  LWM_ERR_TIMEOUT = 7       /* device: an internal pipeline wait exceeded its bound */
+  LWM_ERR_TIMEOUT = 7,      /* device: an internal pipeline wait exceeded its bound */
+  LWM_ERR_LENGTHS = 8,      /* device: a decode kv_len outside [T, S_max] */
+  LWM_ERR_TARGETS = 9       /* device: a packed-loss target outside [0, V) on a weighted token */
 } lwm_status;
 
 /* Bytes of device workspace needed for problems of this shape (0 on bad sizes).
@@ -163,6 +165,99 @@ lwm_status lwm_attn_bwd_stages(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_b
                                int B, int S, int H, int D, unsigned stages, void *workspace,
                                size_t workspace_bytes, lwm_stream stream);
 
+/* Rotary position embedding (RoPE) of q and k: the positional encoding whose base theta
+ * LWM raises with the context length (deep-dive page, section "Stage I：长上下文语言模型";
+ * Tables 11 and 13: theta = 1M at 32K tokens, 10M at 128K/256K, 25M at 512K, 50M at 1M
+ * and in the vision-language stages). The pages name RoPE without a formula; this is
+ * RoPE's published definition: for the token at position p = pos[b, i] and each
+ * adjacent pair (2m, 2m+1) of every head vector, m = 0 .. D/2 - 1,
+ *     angle     = p * theta^(-2m/D)
+ *     y[2m]     = x[2m] cos(angle) - x[2m+1] sin(angle)
+ *     y[2m+1]   = x[2m] sin(angle) + x[2m+1] cos(angle)
+ * With inverse = 1 the pairs are rotated by -angle (the transpose): applied to the
+ * gradients with respect to the rotated q and k, it gives the gradients with respect
+ * to the unrotated ones. Attention with RoPE is therefore: rotate q and k, run
+ * lwm_attn_fwd / lwm_attn_bwd on the rotated tensors (keep them for the backward
+ * pass), then rotate dq and dk back with inverse = 1.
+ *   q, k, q_out, k_out : bf16 [B, S, H, D]; either tensor may be skipped (q and q_out
+ *                        both NULL, or k and k_out both NULL), not both; q_out == q
+ *                        (in place) is allowed, other overlaps are not.
+ *   pos                : int32 [B, S] positions (for packed rows: the offset inside the
+ *                        document, as for lwm_attn_fwd); NULL means pos = i, the index
+ *                        in the row.
+ *   theta              : the base, > 0 and finite.
+ * Angles are reduced in double precision, sin/cos and the rotation run in fp32, and the
+ * result is rounded to bf16. Errors: LWM_ERR_INVALID_ARG (sizes, theta, inverse not
+ * 0/1, pointer pairs), LWM_ERR_UNSUPPORTED (D != 128), LWM_ERR_ALIGNMENT (tensors not
+ * 16-byte or pos not 4-byte aligned). Memory-bound: reads and writes each element
+ * once. */
+lwm_status lwm_attn_rope(const lwm_bf16 *q, const lwm_bf16 *k, const int32_t *pos, double theta,
+                         lwm_bf16 *q_out, lwm_bf16 *k_out, int B, int S, int H, int D, int inverse,
+                         lwm_stream stream);
+
+/* Attention of a few new tokens against a long key/value cache (decoding): the
+ * inference side of the 1M-token context (deep-dive page, section "RingAttention
+ * 为什么必要": 1M-token inference needs at least a v4-128 with 32-way tensor and 4-way
+ * sequence parallelism). Exactly the same attention as lwm_attn_fwd, for the last T
+ * positions of each row only:
+ *   q       : bf16 [B, T, H, D], the queries of the T newest tokens of each row;
+ *   k_cache, v_cache : bf16 [B, S_max, H, D] (the layout of lwm_attn_fwd's k, v); row b
+ *             holds kv_len[b] valid tokens, the T new ones last (positions
+ *             kv_len[b] - T .. kv_len[b] - 1);
+ *   kv_len  : int32 [B] on the device, T <= kv_len[b] <= S_max (NULL: all S_max);
+ *   out     : bf16 [B, T, H, D];  lse : fp32 [B, H, T] (natural log).
+ * Query t of row b (at position P = kv_len[b] - T + t) attends causally to keys
+ * 0 .. P of its row: one document per row (no segments).
+ * The cache is cut into splits of equal length; each split's partial softmax
+ * (running max, sum and unnormalised output) is computed by its own CTA, which stages
+ * the cache through shared memory with bulk copies, and a second kernel merges the
+ * partials by their log-sum-exp: out = sum_s exp(lse_s - lse) out_s. Memory-bound: the
+ * cache is read once. 1 <= T <= 4. The workspace (caller-owned, zero-filled once like
+ * every workspace of this library) holds the partials and an error word:
+ * lwm_attn_decode_workspace_size bytes. A kv_len outside [T, S_max] is reported by
+ * lwm_attn_check as LWM_ERR_LENGTHS (that row's outputs are zero). */
+size_t lwm_attn_decode_workspace_size(int B, int T, int S_max, int H, int D);
+
+lwm_status lwm_attn_decode(const lwm_bf16 *q, const lwm_bf16 *k_cache, const lwm_bf16 *v_cache,
+                           const int32_t *kv_len, lwm_bf16 *out, float *lse, int B, int T, int S_max, int H,
+                           int D, void *workspace, size_t workspace_bytes, lwm_stream stream);
+
+/* Re-weighted cross-entropy of a packed batch: the loss of masked sequence packing
+ * (deep-dive page, section "Masked sequence packing": besides the attention mask, LWM
+ * re-weights the loss so that packed training equals non-packed + padding training;
+ * otherwise the token count of long video samples drowns short answers). The pages
+ * give no formula; the reading here: non-packed, each document is its own row whose
+ * loss is the weighted mean of its token losses, and the batch loss is the mean over
+ * those rows. With documents d (the contiguous runs of equal seg_ids >= 0, as for the
+ * attention), token weights w_t >= 0 and token losses l_t:
+ *     loss = (1/N) sum_d ( sum_{t in d} w_t l_t ) / n_d,    n_d = sum_{t in d} w_t,
+ *     N = number of documents with n_d > 0,  l_t = log sum_v exp(z_t[v]) - z_t[y_t],
+ *     dlogits_t = w_t / (N n_d) (softmax(z_t) - onehot(y_t)).
+ *   logits  : bf16 [B, S, V] (V a multiple of 8), z_t = logits[b, i, :];
+ *   targets : int32 [B, S], y_t (only read where w_t > 0; must lie in [0, V));
+ *   weight  : fp32 [B, S] or NULL (1 everywhere); 0 = no loss on that token (e.g. the
+ *             last token of each document, whose next token belongs to another one);
+ *             negative or non-finite weights count as 0. Padding tokens (seg < 0)
+ *             carry no loss;
+ *   seg_ids : int32 [B, S] or NULL (one document per row);
+ *   loss    : one double on the device (the loss);
+ *   dlogits : bf16 [B, S, V] or NULL (loss only); fully written (zeros where w_t = 0).
+ * Memory-bound: the logits are read once from HBM (a second pass for the gradient
+ * hits L2) and the gradient written once. The loss is summed in a fixed order
+ * (reproducible); the per-document weight sums add fp64 terms atomically, exact for
+ * integer weights such as 0/1 masks. Workspace: lwm_packed_loss_workspace_size bytes,
+ * caller-owned. Device-side errors (seg_ids breaking the packing preconditions, a
+ * target outside [0, V)) are returned by lwm_attn_check(workspace) as LWM_ERR_SEGMENTS
+ * / LWM_ERR_TARGETS. Host-side: LWM_ERR_INVALID_ARG (sizes, NULLs, small workspace),
+ * LWM_ERR_UNSUPPORTED (V not a multiple of 8), LWM_ERR_ALIGNMENT (logits / dlogits not
+ * 16-byte, targets / weight / seg_ids not 4-byte, loss not 8-byte aligned),
+ * LWM_ERR_WORKSPACE (not 256-byte aligned). */
+size_t lwm_packed_loss_workspace_size(int B, int S);
+
+lwm_status lwm_packed_loss(const lwm_bf16 *logits, const int32_t *targets, const float *weight,
+                           const int32_t *seg_ids, double *loss, lwm_bf16 *dlogits, int B, int S, int V,
+                           void *workspace, size_t workspace_bytes, lwm_stream stream);
+
 /* Bytes of the library's own device scratch array used by lwm_attn_fwd_noalloc. */
 #define LWM_NOALLOC_SCRATCH_BYTES (16u << 20)
 
@@ -199,24 +294,25 @@ lwm_status lwm_attn_fwd_noalloc(const lwm_bf16 *q, const lwm_bf16 *k, const lwm_
                                 int B, int S, int H, int D, lwm_stream stream);
 
 /* Synchronises `stream`, then returns and clears the device error word held in
- * `workspace` (LWM_OK, LWM_ERR_SEGMENTS or LWM_ERR_TIMEOUT), or LWM_ERR_CUDA if the
- * stream reported a CUDA error. */
+ * `workspace` (LWM_OK, LWM_ERR_SEGMENTS, LWM_ERR_LENGTHS, LWM_ERR_TARGETS or
+ * LWM_ERR_TIMEOUT), or LWM_ERR_CUDA if the stream reported a CUDA error. */
 lwm_status lwm_attn_check(void *workspace, lwm_stream stream);
 
 /* Bound of the kernels' pipeline waits, for tests of the failure path. Every wait of a
- * kernel role on another role (an mbarrier phase, a counter) gives up after a bound of
- * wall time, sets LWM_ERR_TIMEOUT in the workspace's error word, and the kernel lets
- * copies and products in flight land, frees its tensor memory and returns, so the
- * CUDA context stays usable. The default bound is 2 s, far above any legitimate wait.
- * This call stores `limit_ns` in `workspace` (enqueued on `stream`; 0 restores the
- * default); every later call with that workspace uses it until it is changed. A limit
- * of a few microseconds makes the waits run out on purpose: a test can then check that
- * lwm_attn_check() returns LWM_ERR_TIMEOUT and that the next call with the default
- * bound still computes correct results. The waits that let in-flight work land keep
- * the default bound. Source: none on the LWM pages (failure handling of this
- * library). Returns LWM_ERR_INVALID_ARG for a NULL workspace, LWM_ERR_WORKSPACE for a
- * workspace that is not 256-byte aligned, LWM_ERR_CUDA if the launch fails. */
-lwm_status lwm_attn_set_wait_limit(void *workspace, uint64_t limit_ns, lwm_stream stream);
+ * kernel role on another (an mbarrier phase, a counter) gives up after a bound of wall
+ * time, sets LWM_ERR_TIMEOUT in the workspace's error word, and the kernel lets copies
+ * and products in flight land, frees its tensor memory and returns, so the CUDA
+ * context stays usable. The default bound is 2 s, far above any legitimate wait. This
+ * call sets the bound for every kernel this process launches afterwards, on any
+ * device and stream (0 restores the default; it is read when a call launches its
+ * kernels). A bound below 1 ms is a test setting: each kernel's producer then also
+ * waits once, with its first copies in flight, for a phase that never completes, so a
+ * bound of a few nanoseconds makes that wait run out for certain; a test can then check
+ * that lwm_attn_check() returns LWM_ERR_TIMEOUT and that the next call with the default
+ * bound still computes correct results. The waits that let in-flight work land keep the
+ * default bound. Source: none on the LWM pages (failure handling of this library).
+ * Always returns LWM_OK. */
+lwm_status lwm_attn_set_wait_limit(uint64_t limit_ns);
 
 /* Description of the most recent LWM_ERR_CUDA raised on the calling host thread: the
  * failing call and the CUDA error text ("" if none). The string is owned by the

@@ -36,27 +36,37 @@ def _fwd_bwd(x, ws):
     return st_fwd, st_bwd, (out, lse, dq, dk, dv)
 
 
-def test_expired_wait_is_reported_and_the_context_stays_usable(cuda_device):
+@pytest.fixture
+def short_wait_bound():
+    """Sets the process-wide wait bound to 1 ns (a wait not satisfied at once gives up) and
+    restores the default afterwards, whatever the test's outcome."""
+    lwm.lwm_attn_set_wait_limit(1)
+    try:
+        yield
+    finally:
+        lwm.lwm_attn_set_wait_limit(0)
+
+
+def test_expired_wait_is_reported_and_the_context_stays_usable(cuda_device, short_wait_bound):
     w = I.workload(1)                     # packed 300/424/300, S = 1K, H = 4
     x = I.make_inputs(w, cuda_device)
     ws = lwm.new_workspace(w.B, w.S, w.H, w.D, cuda_device)
-    lwm.lwm_attn_set_wait_limit(ws, 1)    # 1 ns: a wait not satisfied at once gives up
     st_fwd, st_bwd, _ = _fwd_bwd(x, ws)
     assert st_fwd == TIMEOUT and st_bwd == TIMEOUT, (st_fwd, st_bwd)
     # the fused backward kernel takes the same path
     out = torch.empty_like(x["q"])
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=cuda_device)
-    lwm.lwm_attn_set_wait_limit(ws, 0)
+    lwm.lwm_attn_set_wait_limit(0)
     lwm.lwm_attn_fwd(x["q"], x["k"], x["v"], x["seg"], x["pos"], out, lse, ws)
     assert lwm.lwm_attn_check(ws) == 0
-    lwm.lwm_attn_set_wait_limit(ws, 1)
+    lwm.lwm_attn_set_wait_limit(1)
     dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
     lwm.lwm_attn_bwd_stages(x["q"], x["k"], x["v"], out, x["dout"], lse, dq, dk, dv,
                             lwm.LWM_BWD_DELTA | lwm.LWM_BWD_FUSED, ws)
     assert lwm.lwm_attn_check(ws) == TIMEOUT
 
     # default bound again: same context, same workspace, correct results
-    lwm.lwm_attn_set_wait_limit(ws, 0)
+    lwm.lwm_attn_set_wait_limit(0)
     st_fwd, st_bwd, (out, lse, dq, dk, dv) = _fwd_bwd(x, ws)
     assert st_fwd == 0 and st_bwd == 0
     seg = x["seg"].cpu().numpy()
