@@ -428,7 +428,8 @@ lwm_status lwm_packed_loss(const lwm_bf16 *logits, const int32_t *targets, const
   if (workspace_bytes < need) return LWM_ERR_INVALID_ARG;
   DeviceInfo d;
   LWM_TRY(device_info(d));
-  return from_cuda(launch_packed_loss(logits, targets, weight, seg_ids, loss, dlogits, B, S, V, workspace, stream));
+  return from_cuda(
+      launch_packed_loss(logits, targets, weight, seg_ids, loss, dlogits, B, S, V, workspace, d.num_sms, stream));
 }
 
 lwm_status lwm_attn_set_wait_limit(uint64_t limit_ns) {

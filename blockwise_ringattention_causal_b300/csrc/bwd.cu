@@ -214,15 +214,17 @@ struct KvbBars {
   uint64_t pt_free, ds_free;          // dV / dK product done with PT / DS
   uint64_t acc_full, acc_empty;
   uint64_t item_full[2], item_empty[2];
-  uint64_t drain, never;
+  uint64_t drain;
   int item[2];
   uint32_t tmem_base;
   WaitCtl ctl;
   int fill, use, own_issued, own_used;
+  uint64_t never;   // the failure test's wait (test instantiation only)
 };
 constexpr int KVB_SMEM = KVB_SM_BAR + int(sizeof(KvbBars)) + 1024;
 static_assert(KVB_SMEM <= 232448, "shared memory budget of one CTA");
 
+template <bool TEST>
 __device__ __forceinline__ bool kv_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                                             const CUtensorMap *tdo, const BwArgs &a, uint8_t *smem, KvbBars *bars) {
   WaitCtl *abort = &bars->ctl;
@@ -259,7 +261,9 @@ __device__ __forceinline__ bool kv_producer(const CUtensorMap *tq, const CUtenso
       ++fill;
     }
     if (!ok) break;
-    if (a.wait.test && it == 0 && !(ok = test_expiry_wait(&bars->never, abort))) break;
+    if constexpr (TEST) {
+      if (it == 0 && !(ok = test_expiry_wait(&bars->never, abort))) break;
+    }
   }
   bars->fill = fill;
   bars->own_issued = own;
@@ -528,6 +532,7 @@ __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBa
   return ok;
 }
 
+template <bool TEST>
 __global__ void __launch_bounds__(BW_THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const BwArgs a) {
@@ -555,7 +560,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 2);
-    mbar_init(&bars->never, 1);
+    if (TEST) mbar_init(&bars->never, 1);
     bars->ctl.init(a.wait);
     bars->fill = bars->use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
@@ -578,7 +583,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   if (warp < BW_PRODUCER) {
     ok = kv_softmax(a, smem, bars, tmem, warp >> 2, warp, lane);
   } else if (warp == BW_PRODUCER) {
-    if (lane == 0) ok = kv_producer(&tq, &tk, &tv, &tdo, a, smem, bars);
+    if (lane == 0) ok = kv_producer<TEST>(&tq, &tk, &tv, &tdo, a, smem, bars);
     __syncwarp();
   } else if (warp == BW_MMA) {
     ok = kv_x_issuer(a, smem, bars, tmem, lane);
@@ -644,15 +649,17 @@ struct DqBars {
   uint64_t a_free[2];   // dQ(j) has completed: slot A_{j % 2} may take S(j + 2)
   uint64_t acc_full, acc_empty;
   uint64_t item_full[2], item_empty[2];
-  uint64_t drain, never;
+  uint64_t drain;
   int item[2];
   uint32_t tmem_base;
   WaitCtl ctl;
   int k_fill, k_use, v_fill, v_use, own_issued, own_used;
+  uint64_t never;   // the failure test's wait (test instantiation only)
 };
 constexpr int DQ_SMEM = DQ_SM_BAR + int(sizeof(DqBars)) + 1024;
 static_assert(DQ_SMEM <= 232448, "shared memory budget of one CTA");
 
+template <bool TEST>
 __device__ __forceinline__ bool dq_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                                             const CUtensorMap *tdo, const BwArgs &a, uint8_t *smem, DqBars *bars) {
   WaitCtl *abort = &bars->ctl;
@@ -691,7 +698,9 @@ __device__ __forceinline__ bool dq_producer(const CUtensorMap *tq, const CUtenso
     if (!ok) break;
     // failure test only: wait, with this item's copies and products in flight, for a
     // phase that never completes (the short test bound makes the wait run out)
-    if (a.wait.test && it == 0 && !(ok = test_expiry_wait(&bars->never, abort))) break;
+    if constexpr (TEST) {
+      if (it == 0 && !(ok = test_expiry_wait(&bars->never, abort))) break;
+    }
   }
   bars->k_fill = k_fill;
   bars->v_fill = v_fill;
@@ -912,6 +921,7 @@ __device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32
   return ok;
 }
 
+template <bool TEST>
 __global__ void __launch_bounds__(BW_THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const BwArgs a) {
@@ -943,7 +953,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 3);
-    mbar_init(&bars->never, 1);
+    if (TEST) mbar_init(&bars->never, 1);
     bars->ctl.init(a.wait);
     bars->k_fill = bars->k_use = bars->v_fill = bars->v_use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
@@ -966,7 +976,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   if (warp < BW_PRODUCER) {
     ok = dq_softmax(a, bars, tmem, warp >> 2, warp, lane);
   } else if (warp == BW_PRODUCER) {
-    if (lane == 0) ok = dq_producer(&tq, &tk, &tv, &tdo, a, smem, bars);
+    if (lane == 0) ok = dq_producer<TEST>(&tq, &tk, &tv, &tdo, a, smem, bars);
     __syncwarp();
   } else if (warp == BW_MMA || warp == BW_MMA2 || warp == BW_MMA3) {
     ok = dq_mma(a, smem, bars, tmem, warp - BW_MMA, lane);
@@ -1034,9 +1044,12 @@ BwArgs bw_args(const Problem &p, void *workspace, const int *list) {
 
 cudaError_t launch_dkdv(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                         void *dk, void *dv, const Problem &p, void *workspace, cudaStream_t stream) {
-  static std::atomic<uint64_t> attr_done{0};
+  static std::atomic<uint64_t> attr_done[2] = {{0}, {0}};
+  const bool test = wait_bound().test != 0;
   {
-    const cudaError_t e = smem_attr_once(reinterpret_cast<const void *>(dkdv_kernel), KVB_SMEM, attr_done);
+    const void *kern = test ? reinterpret_cast<const void *>(dkdv_kernel<true>)
+                            : reinterpret_cast<const void *>(dkdv_kernel<false>);
+    const cudaError_t e = smem_attr_once(kern, KVB_SMEM, attr_done[test ? 1 : 0]);
     if (e != cudaSuccess) return e;
   }
   const Workspace w = Workspace::layout(p.B, p.S, p.H);
@@ -1044,22 +1057,27 @@ cudaError_t launch_dkdv(const CUtensorMap &tq, const CUtensorMap &tk, const CUte
   a.out0 = static_cast<__nv_bfloat16 *>(dv);
   a.out1 = static_cast<__nv_bfloat16 *>(dk);
   const int grid = a.n_items < p.num_sms ? a.n_items : p.num_sms;
-  dkdv_kernel<<<grid, BW_THREADS, KVB_SMEM, stream>>>(tq, tk, tv, tdo, a);
+  if (test) dkdv_kernel<true><<<grid, BW_THREADS, KVB_SMEM, stream>>>(tq, tk, tv, tdo, a);
+  else dkdv_kernel<false><<<grid, BW_THREADS, KVB_SMEM, stream>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                       void *dq, const Problem &p, void *workspace, cudaStream_t stream) {
-  static std::atomic<uint64_t> attr_done{0};
+  static std::atomic<uint64_t> attr_done[2] = {{0}, {0}};
+  const bool test = wait_bound().test != 0;
   {
-    const cudaError_t e = smem_attr_once(reinterpret_cast<const void *>(dq_kernel), DQ_SMEM, attr_done);
+    const void *kern = test ? reinterpret_cast<const void *>(dq_kernel<true>)
+                            : reinterpret_cast<const void *>(dq_kernel<false>);
+    const cudaError_t e = smem_attr_once(kern, DQ_SMEM, attr_done[test ? 1 : 0]);
     if (e != cudaSuccess) return e;
   }
   const Workspace w = Workspace::layout(p.B, p.S, p.H);
   BwArgs a = bw_args(p, workspace, reinterpret_cast<const int *>(static_cast<char *>(workspace) + w.off_list_q));
   a.out0 = static_cast<__nv_bfloat16 *>(dq);
   const int grid = a.n_items < p.num_sms ? a.n_items : p.num_sms;
-  dq_kernel<<<grid, BW_THREADS, DQ_SMEM, stream>>>(tq, tk, tv, tdo, a);
+  if (test) dq_kernel<true><<<grid, BW_THREADS, DQ_SMEM, stream>>>(tq, tk, tv, tdo, a);
+  else dq_kernel<false><<<grid, BW_THREADS, DQ_SMEM, stream>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 }  // namespace lwm

@@ -71,11 +71,12 @@ struct FbBars {
   uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty;
   uint64_t acc_full, acc_empty;
   uint64_t item_full[2], item_empty[2];
-  uint64_t drain, never;
+  uint64_t drain;
   int item[2];
   uint32_t tmem_base;
   WaitCtl ctl;
   int q_fill, q_use, do_fill, do_use, own_issued, own_used;
+  uint64_t never;   // the failure test's wait (test instantiation only)
 };
 constexpr int FB_SMEM = FB_SM_BAR + int(sizeof(FbBars)) + 1024;
 static_assert(FB_SMEM <= 232448, "shared memory budget of one CTA");
@@ -176,6 +177,7 @@ __device__ __forceinline__ void fb_load_tile(const CUtensorMap *m, uint64_t *bar
 }
 
 // ----------------------------------------------------------------------------- producer
+template <bool TEST>
 __device__ __forceinline__ bool fb_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                                             const CUtensorMap *tdo, const FbArgs &a, uint8_t *smem, FbBars *bars) {
   WaitCtl *abort = &bars->ctl;
@@ -217,7 +219,9 @@ __device__ __forceinline__ bool fb_producer(const CUtensorMap *tq, const CUtenso
     if (!ok) break;
     // failure test only: wait, with this item's copies and products in flight, for a
     // phase that never completes (the short test bound makes the wait run out)
-    if (a.wait.test && it == 0 && !(ok = test_expiry_wait(&bars->never, abort))) break;
+    if constexpr (TEST) {
+      if (it == 0 && !(ok = test_expiry_wait(&bars->never, abort))) break;
+    }
   }
   bars->q_fill = q_fill;
   bars->do_fill = do_fill;
@@ -545,6 +549,7 @@ __device__ __forceinline__ void fb_finish(bool ok, const FbArgs &a, FbBars *bars
   }
 }
 
+template <bool TEST>
 __global__ void __launch_bounds__(FB_THREADS, 1)
     dkdvq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -574,7 +579,7 @@ __global__ void __launch_bounds__(FB_THREADS, 1)
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 1);
-    mbar_init(&bars->never, 1);
+    if (TEST) mbar_init(&bars->never, 1);
     bars->ctl.init(a.wait);
     bars->q_fill = bars->q_use = bars->do_fill = bars->do_use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
@@ -599,7 +604,7 @@ __global__ void __launch_bounds__(FB_THREADS, 1)
   if (warp < FB_PRODUCER) {
     ok = fb_softmax(&tdq, a, smem, bars, tmem, warp >> 2, warp, lane);
   } else if (warp == FB_PRODUCER) {
-    if (lane == 0) ok = fb_producer(&tq, &tk, &tv, &tdo, a, smem, bars);
+    if (lane == 0) ok = fb_producer<TEST>(&tq, &tk, &tv, &tdo, a, smem, bars);
     __syncwarp();
   } else if (warp == FB_MMA) {
     ok = fb_mma(a, smem, bars, tmem, lane);
@@ -635,9 +640,12 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float4 *__restric
 cudaError_t launch_dkdvq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                          const CUtensorMap &tdqacc, void *dq, void *dk, void *dv, const Problem &p, void *workspace,
                          cudaStream_t stream) {
-  static std::atomic<uint64_t> attr_done{0};
+  static std::atomic<uint64_t> attr_done[2] = {{0}, {0}};
+  const bool test = wait_bound().test != 0;
   {
-    const cudaError_t e = smem_attr_once(reinterpret_cast<const void *>(dkdvq_kernel), FB_SMEM, attr_done);
+    const void *kern = test ? reinterpret_cast<const void *>(dkdvq_kernel<true>)
+                            : reinterpret_cast<const void *>(dkdvq_kernel<false>);
+    const cudaError_t e = smem_attr_once(kern, FB_SMEM, attr_done[test ? 1 : 0]);
     if (e != cudaSuccess) return e;
   }
   const Workspace w = Workspace::layout(p.B, p.S, p.H);
@@ -665,7 +673,8 @@ cudaError_t launch_dkdvq(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   cudaError_t e = cudaMemsetAsync(dqacc, 0, w.dqacc_bytes, stream);
   if (e != cudaSuccess) return e;
   const int grid = a.n_items < p.num_sms ? a.n_items : p.num_sms;
-  dkdvq_kernel<<<grid, FB_THREADS, FB_SMEM, stream>>>(tq, tk, tv, tdo, tdqacc, a);
+  if (test) dkdvq_kernel<true><<<grid, FB_THREADS, FB_SMEM, stream>>>(tq, tk, tv, tdo, tdqacc, a);
+  else dkdvq_kernel<false><<<grid, FB_THREADS, FB_SMEM, stream>>>(tq, tk, tv, tdo, tdqacc, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long total = (long long)p.B * p.S * p.H * (HD / 8);

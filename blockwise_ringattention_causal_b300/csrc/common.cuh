@@ -162,11 +162,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // waits run out; the fast path of a wait is a single try_wait on the barrier.
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s: far above any legitimate wait
 
-// Bounds below this are test settings (the failure test): a wait whose first try_wait
-// fails then reads the clock on every poll, and each kernel's producer waits once, with
-// work in flight, for a phase that never completes (test_expiry_wait), so that the bound
-// runs out for certain. A suspending try_wait usually sees a real phase complete before
-// any clock check, so shortening the bound alone would not make waits run out.
+// Bounds below this are test settings (the failure test): the host then launches each
+// kernel's test instantiation, whose producer waits once, with work in flight, for a
+// phase that never completes (test_expiry_wait), so that the bound runs out for certain.
+// A suspending try_wait usually sees a real phase complete before any clock check, so
+// shortening the bound alone would not make waits run out. The production
+// instantiations contain no test code at all (it would shift their code layout).
 constexpr uint64_t SHORT_WAIT_LIMIT_NS = 1000000ull;
 
 // The bound as a kernel launch parameter.
@@ -187,28 +188,30 @@ struct WaitCtl {
 };
 
 // The fast path is one (suspending) try_wait; only after it fails are the abort flag and
-// the clock consulted: every 64 polls, or on every poll under a test bound.
+// the clock consulted, every 64 polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, WaitCtl *ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   const uint64_t limit = ctl->limit_ns;
-  const uint32_t check = limit < SHORT_WAIT_LIMIT_NS ? 0u : 63u;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & check) == 0u) {
+    if ((it & 63u) == 0u) {
       if (*reinterpret_cast<volatile int *>(&ctl->abort)) return false;
       if (global_timer_ns() - t0 > limit) return false;
     }
   }
 }
 
-// The failure test's wait: a phase that nothing ever completes (an mbarrier that no
-// thread arrives on), waited for under the test's short bound, at a point where copies
-// and products are in flight, so that the abort path has real work to let land.
-// Out of line: it sits on the producers' cold path only, and inlining it would change
-// the register allocation of the whole kernel.
-static __device__ __noinline__ bool test_expiry_wait(uint64_t *never, WaitCtl *ctl) {
-  return mbar_wait(never, 0, ctl);
+// The failure test's wait, compiled only into the kernels' test instantiations: a phase
+// that nothing ever completes (an mbarrier that no thread arrives on), waited for under
+// the test's short bound, with the clock read on every poll, at a point where copies and
+// products are in flight, so that the abort path has real work to let land.
+__device__ __forceinline__ bool test_expiry_wait(uint64_t *never, WaitCtl *ctl) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(never, 0)) return true;
+    if (global_timer_ns() - t0 > ctl->limit_ns) return false;
+  }
 }
 
 // Spins (bounded like mbar_wait) until *count reaches target.

@@ -66,7 +66,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float *f) {
   }
 }
 
-template <int T>
+template <int T, bool TEST>
 __global__ void __launch_bounds__(DEC_THREADS, 1) decode_split_kernel(const __grid_constant__ DecArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_split_kernel(const __gr
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], DEC_CWARPS);
     }
-    mbar_init(&bars->never, 1);
+    if (TEST) mbar_init(&bars->never, 1);
     bars->ctl.init(a.wait);
     bars->fill = bars->seen = 0;
     fence_mbar_init();
@@ -115,7 +115,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_split_kernel(const __gr
         }
         ++fill;
         // failure test only: a phase that never completes, with this stage's copies in flight
-        if (a.wait.test && st == 0 && !(ok = test_expiry_wait(&bars->never, ctl))) break;
+        if constexpr (TEST) {
+          if (st == 0 && !(ok = test_expiry_wait(&bars->never, ctl))) break;
+        }
       }
       bars->fill = fill;
     }
@@ -315,10 +317,13 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const int
   switch (T) {
 #define LWM_DECODE_CASE(TT)                                                                                     \
   case TT: {                                                                                                    \
-    static std::atomic<uint64_t> attr_done{0};                                                                  \
-    e = smem_attr_once(reinterpret_cast<const void *>(decode_split_kernel<TT>), DEC_SMEM, attr_done);            \
+    static std::atomic<uint64_t> attr_done[2] = {{0}, {0}};                                                     \
+    const void *kern = a.wait.test ? reinterpret_cast<const void *>(decode_split_kernel<TT, true>)              \
+                                   : reinterpret_cast<const void *>(decode_split_kernel<TT, false>);            \
+    e = smem_attr_once(kern, DEC_SMEM, attr_done[a.wait.test ? 1 : 0]);                                         \
     if (e != cudaSuccess) return e;                                                                             \
-    decode_split_kernel<TT><<<grid, DEC_THREADS, DEC_SMEM, stream>>>(a);                                        \
+    if (a.wait.test) decode_split_kernel<TT, true><<<grid, DEC_THREADS, DEC_SMEM, stream>>>(a);                 \
+    else decode_split_kernel<TT, false><<<grid, DEC_THREADS, DEC_SMEM, stream>>>(a);                            \
     break;                                                                                                      \
   }
     LWM_DECODE_CASE(1)

@@ -46,12 +46,13 @@ struct FwdBars {
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_free, p_full[2], pv_done[2], o_empty[2];
   uint64_t item_full[2], item_empty[2];
-  uint64_t drain, never;
+  uint64_t drain;
   int item[2];
   uint32_t tmem_base;
   WaitCtl ctl;
   int kv_fill, kv_use_k, kv_use_v[2], q_issued, q_used;
   int s_issued[2];   // S products of query tile t issued so far
+  uint64_t never;    // the failure test's wait (test instantiation only)
 };
 
 constexpr int FWD_SMEM = SM_BAR + int(sizeof(FwdBars)) + 1024;   // + alignment slack
@@ -130,6 +131,7 @@ __device__ __forceinline__ Ranges item_ranges(const FwdArgs &a, const Item &I) {
 }
 
 // ----------------------------------------------------------------------------- producer
+template <bool TEST>
 __device__ bool producer_role(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                               const FwdArgs &a, uint8_t *smem, FwdBars *bars, int kv_chunk) {
   WaitCtl *abort = &bars->ctl;
@@ -169,7 +171,9 @@ __device__ bool producer_role(const CUtensorMap *tq, const CUtensorMap *tk, cons
     if (!ok) break;
     // failure test only: wait, with this item's copies and products in flight, for a
     // phase that never completes (the short test bound makes the wait run out)
-    if (a.wait.test && it == 0 && !(ok = test_expiry_wait(&bars->never, abort))) break;
+    if constexpr (TEST) {
+      if (it == 0 && !(ok = test_expiry_wait(&bars->never, abort))) break;
+    }
   }
   bars->kv_fill = kv_fill;
   bars->q_issued = q_issued;
@@ -463,6 +467,7 @@ __device__ bool softmax_role(const FwdArgs &a, FwdBars *bars, uint32_t tmem, int
   return ok;
 }
 
+template <bool TEST>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
@@ -489,7 +494,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       mbar_init(&bars->item_empty[t], 11);   // softmax 8 + MMA 3 warps
     }
     mbar_init(&bars->drain, 3);
-    mbar_init(&bars->never, 1);
+    if (TEST) mbar_init(&bars->never, 1);
     bars->ctl.init(a.wait);
     bars->kv_fill = bars->kv_use_k = bars->kv_use_v[0] = bars->kv_use_v[1] = bars->q_issued = bars->q_used = 0;
     bars->s_issued[0] = bars->s_issued[1] = 0;
@@ -511,7 +516,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 
   bool ok = true;
   if (warp == WARP_PRODUCER) {
-    if (lane == 0) ok = producer_role(&tq, &tk, &tv, a, smem, bars, kv_chunk);
+    if (lane == 0) ok = producer_role<TEST>(&tq, &tk, &tv, a, smem, bars, kv_chunk);
     __syncwarp();
   } else if (warp == WARP_MMA) {
     ok = s_issuer_role(a, smem, bars, tmem, kv_chunk, lane);
@@ -562,9 +567,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, void *out,
                        float *lse, const Problem &p, void *workspace, cudaStream_t stream) {
-  static std::atomic<uint64_t> attr_done{0};
+  static std::atomic<uint64_t> attr_done[2] = {{0}, {0}};
+  const WaitBound wb = wait_bound();
+  const void *kern = wb.test ? reinterpret_cast<const void *>(fwd_kernel<true>)
+                             : reinterpret_cast<const void *>(fwd_kernel<false>);
   {
-    const cudaError_t e = smem_attr_once(reinterpret_cast<const void *>(fwd_kernel), FWD_SMEM, attr_done);
+    const cudaError_t e = smem_attr_once(kern, FWD_SMEM, attr_done[wb.test ? 1 : 0]);
     if (e != cudaSuccess) return e;
   }
   const Workspace w = Workspace::layout(p.B, p.S, p.H);
@@ -583,9 +591,10 @@ cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   a.n_list = p.B * w.nP;
   a.n_items = a.n_list * p.H;
   a.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
-  a.wait = wait_bound();
+  a.wait = wb;
   const int grid = a.n_items < p.num_sms ? a.n_items : p.num_sms;
-  fwd_kernel<<<grid, FWD_THREADS, FWD_SMEM, stream>>>(tq, tk, tv, a);
+  if (wb.test) fwd_kernel<true><<<grid, FWD_THREADS, FWD_SMEM, stream>>>(tq, tk, tv, a);
+  else fwd_kernel<false><<<grid, FWD_THREADS, FWD_SMEM, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 

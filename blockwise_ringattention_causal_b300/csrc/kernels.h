@@ -77,7 +77,7 @@ struct LossLayout {
 };
 LossLayout loss_layout(int B, int S);
 cudaError_t launch_packed_loss(const void *logits, const int *targets, const float *weight, const int *seg,
-                               double *loss, void *dlogits, int B, int S, int V, void *workspace,
+                               double *loss, void *dlogits, int B, int S, int V, void *workspace, int num_sms,
                                cudaStream_t stream);
 
 }  // namespace lwm

@@ -12,10 +12,10 @@
 //
 // Kernels (all memory-bound): document starts from seg (the metadata pre-pass's first
 // pass), per-document weight sums (fp64; one atomic per document and CTA), the count
-// N, then one warp per token row: an online max / sum over the row's logits (16-byte
-// loads, four in flight per lane), the row's loss term, and the gradient row written
-// from a second pass over the logits (an L2 hit for the rows in flight). The loss is
-// summed per CTA and the CTA sums in a fixed order: deterministic for a given input.
+// N, then the rows: for vocabularies up to 48K, one CTA per row with the row staged
+// once in shared memory by a bulk copy (an online max / sum pass and the gradient pass
+// both read it there); beyond that, one warp per row reading the logits twice. The loss
+// is summed per CTA and the CTA sums in a fixed order: deterministic for a given input.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -102,6 +102,7 @@ struct CeArgs {
   double *part;              // one loss term per CTA
   int *err;
   int B, S, S_pad, V;
+  WaitBound wait;
 };
 
 __device__ __forceinline__ void bf16x8(const uint4 &u, float *f) {
@@ -211,6 +212,138 @@ __global__ void __launch_bounds__(CE_WARPS * 32) ce_kernel(const __grid_constant
   }
 }
 
+// One CTA per token row (persistent over rows r = blockIdx.x + k gridDim.x), for
+// vocabularies whose row fits shared memory: the row is bulk-copied once, then the max /
+// sum pass and the gradient pass both read it from shared memory, so HBM sees each logit
+// read once (the warp-per-row kernel above re-reads its row, from HBM once the rows in
+// flight outgrow L2).
+constexpr int CE_ROW_THREADS = 256;
+constexpr int CE_ROW_MAX_BYTES = 96 * 1024;   // two CTAs per SM
+
+__device__ __forceinline__ float block_sum_256(float v, float *red) {
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int k = 0; k < CE_ROW_THREADS / 32; ++k) t += red[k];
+  __syncthreads();
+  return t;
+}
+
+__device__ __forceinline__ float block_max_256(float v, float *red) {
+  for (int d = 16; d > 0; d >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = red[0];
+#pragma unroll
+  for (int k = 1; k < CE_ROW_THREADS / 32; ++k) t = fmaxf(t, red[k]);
+  __syncthreads();
+  return t;
+}
+
+__global__ void __launch_bounds__(CE_ROW_THREADS, 2) ce_row_kernel(const __grid_constant__ CeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint4 *row = reinterpret_cast<uint4 *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ uint64_t full;
+  __shared__ WaitCtl ctl;
+  __shared__ float red[CE_ROW_THREADS / 32];
+  __shared__ double wp_s;
+  __shared__ bool ok_s;
+  constexpr float LOG2E = 1.4426950408889634f;
+  const long long N = (long long)a.B * a.S;
+  const int nv = a.V / 8;
+  if (threadIdx.x == 0) {
+    mbar_init(&full, 1);
+    ctl.init(a.wait);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  double contrib = 0.0;   // thread 0's running sum of this CTA's rows
+  uint32_t phase = 0;
+  bool ok = true;
+  for (long long r = blockIdx.x; r < N; r += gridDim.x) {
+    if (threadIdx.x == 0) {
+      const int b = int(r / a.S), t = int(r % a.S);
+      double wp = 0.0;
+      const float w = token_weight(a.seg, a.weight, size_t(r));
+      if (w > 0.f) {
+        const int y = a.targets[r];
+        const double nd = a.doc_sum[size_t(b) * a.S_pad + a.lo[size_t(b) * a.S_pad + t]];
+        const int nds = *a.ndocs;
+        if (y < 0 || y >= a.V) raise_error(a.err, ERRBIT_TARGETS);
+        else if (nd > 0.0 && nds > 0) wp = double(w) / (nd * double(nds));
+      }
+      wp_s = wp;
+      if (wp != 0.0) {
+        mbar_arrive_expect_tx(&full, uint32_t(a.V) * 2u);
+        bulk_load(row, a.logits + size_t(r) * nv, uint32_t(a.V) * 2u, &full);
+      }
+    }
+    __syncthreads();
+    const double wp = wp_s;
+    uint4 *gr = a.dlogits ? a.dlogits + size_t(r) * nv : nullptr;
+    if (wp == 0.0) {
+      if (gr)
+        for (int v = threadIdx.x; v < nv; v += CE_ROW_THREADS) gr[v] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+      continue;
+    }
+    // thread 0 waits for the row (and, if the wait ran out, lets the copy land before the
+    // CTA leaves); the block barrier then orders the row before every thread's reads
+    if (threadIdx.x == 0) {
+      ok_s = mbar_wait(&full, phase, &ctl);
+      if (!ok_s) bounded_wait_plain(&full, phase);
+    }
+    __syncthreads();
+    if (!(ok = ok_s)) break;
+    phase ^= 1;
+    float m = -__builtin_huge_valf(), sum = 0.f;
+    for (int v = threadIdx.x; v < nv; v += CE_ROW_THREADS) {
+      float f[8];
+      bf16x8(row[v], f);
+      float mx = f[0];
+#pragma unroll
+      for (int e = 1; e < 8; ++e) mx = fmaxf(mx, f[e]);
+      mx *= LOG2E;
+      if (mx > m) {
+        sum *= ex2_approx(m - mx);
+        m = mx;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum += ex2_approx(fmaf(f[e], LOG2E, -m));
+    }
+    const float M = block_max_256(m, red);
+    const float tot = block_sum_256(m == -__builtin_huge_valf() ? 0.f : sum * ex2_approx(m - M), red);
+    const float lse2 = M + __log2f(tot);
+    const int y = a.targets[r];
+    if (threadIdx.x == 0) {
+      const float zy = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(row)[y]);
+      contrib += wp * (double(lse2) * 0.6931471805599453 - double(zy));
+    }
+    if (gr) {
+      const float g = float(wp);
+      for (int v = threadIdx.x; v < nv; v += CE_ROW_THREADS) {
+        float f[8];
+        bf16x8(row[v], f);
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          float p0 = ex2_approx(fmaf(f[e], LOG2E, -lse2));
+          float p1 = ex2_approx(fmaf(f[e + 1], LOG2E, -lse2));
+          if (8 * v + e == y) p0 -= 1.f;
+          if (8 * v + e + 1 == y) p1 -= 1.f;
+          o[e / 2] = pack_bf16x2(g * p0, g * p1);
+        }
+        gr[v] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    __syncthreads();   // the row buffer is reused by the next row's copy
+  }
+  if (!ok && threadIdx.x == 0) raise_error(a.err, ERRBIT_TIMEOUT);
+  if (threadIdx.x == 0) a.part[blockIdx.x] = contrib;
+}
+
 // The loss: the CTAs' terms summed in a fixed order.
 __global__ void __launch_bounds__(LOSS_THREADS) loss_sum_kernel(const double *__restrict__ part, int n,
                                                                 double *__restrict__ loss) {
@@ -247,7 +380,7 @@ LossLayout loss_layout(int B, int S) {
 }
 
 cudaError_t launch_packed_loss(const void *logits, const int *targets, const float *weight, const int *seg,
-                               double *loss, void *dlogits, int B, int S, int V, void *workspace,
+                               double *loss, void *dlogits, int B, int S, int V, void *workspace, int num_sms,
                                cudaStream_t stream) {
   const LossLayout l = loss_layout(B, S);
   char *base = static_cast<char *>(workspace);
@@ -278,8 +411,22 @@ cudaError_t launch_packed_loss(const void *logits, const int *targets, const flo
   a.S = S;
   a.S_pad = l.S_pad;
   a.V = V;
-  ce_kernel<<<l.n_cta, CE_WARPS * 32, 0, stream>>>(a);
-  loss_sum_kernel<<<1, LOSS_THREADS, 0, stream>>>(a.part, l.n_cta, loss);
+  a.wait = wait_bound();
+  int n_part = l.n_cta;
+  if (V * 2 <= CE_ROW_MAX_BYTES) {
+    static std::atomic<uint64_t> attr_done{0};
+    const int smem = CE_ROW_MAX_BYTES + 128;
+    if ((e = smem_attr_once(reinterpret_cast<const void *>(ce_row_kernel), smem, attr_done)) != cudaSuccess) return e;
+    const long long rows = (long long)B * S;
+    long long grid = (long long)num_sms * 2;
+    if (grid > rows) grid = rows;
+    if (grid > l.n_cta) grid = l.n_cta;
+    n_part = int(grid);
+    ce_row_kernel<<<n_part, CE_ROW_THREADS, smem, stream>>>(a);
+  } else {
+    ce_kernel<<<l.n_cta, CE_WARPS * 32, 0, stream>>>(a);
+  }
+  loss_sum_kernel<<<1, LOSS_THREADS, 0, stream>>>(a.part, n_part, loss);
   return cudaGetLastError();
 }
 
