@@ -308,7 +308,8 @@ def run_ours(args, rank, world):
                 "frac_of_sustained": achieved / peaks["bf16_sustained"] if peaks["bf16_sustained"] else None,
                 "kernel_ms": {n: round(t, 4) for n, t in per_kernel.items()}}
     if w.backward:
-        delta_bytes = B * S * H * D * 2 * 2 + B * H * S * 4 * 3   # read out, dout, lse; write delta, lse2
+        # read out, dout, lse; write delta, lse2 and the two 16-byte offset rows of the dK/dV kernel
+        delta_bytes = B * S * H * D * 2 * 2 + B * H * S * 4 * 3 + B * H * S * 32
         roofline["delta_prepass_gbs"] = delta_bytes / (per_kernel["delta"] * 1e-3) / 1e9
         roofline["delta_prepass_frac_hbm"] = roofline["delta_prepass_gbs"] / peaks["hbm"]
 

@@ -16,15 +16,34 @@ namespace {
 
 constexpr int DELTA_THREADS = 256;
 
+// x as hi + mid + lo in bf16 (each the rounding of what is left): the sum carries about
+// 24 bits, as an fp32 value does; products with 1 are exact in the tensor core.
+__device__ __forceinline__ uint4 bf16_split_row(float x) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+  __nv_bfloat162 a, b;
+  a.x = hi;
+  a.y = mid;
+  b.x = lo;
+  b.y = __float2bfloat16_rn(0.f);
+  return make_uint4(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b), 0u, 0u);
+}
+
 // delta[b,h,i] = sum_d dout[b,i,h,d] * out[b,i,h,d] (fp32), and lse2[b,h,i] =
 // lse * log2(e) on a row stride padded to a multiple of 128, with +inf for rows that
-// see no key (padding) and for the pad tail, so that exp2(s - lse2) is 0 there.
+// see no key (padding) and for the pad tail, so that exp2(s - lse2) is 0 there. Also,
+// for the dK/dV kernel, the offset rows qx = -lse * sqrt(D) (so that (S^T + qx) * c =
+// S^T c - lse2 with c = log2(e) / sqrt(D); -1e30 where nothing is visible) and dox =
+// -delta, each as three bf16 parts in a 16-byte row (see the dK/dV kernel).
 // One warp handles 32 consecutive rows of one head: two rows per load step, 16 lanes
 // per 256-byte row, fully coalesced; the 32 results are written as one 128-byte line.
 __global__ void __launch_bounds__(DELTA_THREADS) delta_kernel(const uint4 *__restrict__ out,
                                                               const uint4 *__restrict__ dout,
                                                               const float *__restrict__ lse,
                                                               float *__restrict__ delta, float *__restrict__ lse2,
+                                                              uint4 *__restrict__ qx, uint4 *__restrict__ dox,
                                                               int B, int S, int H, int S_pad) {
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * (DELTA_THREADS / 32);
@@ -64,12 +83,18 @@ __global__ void __launch_bounds__(DELTA_THREADS) delta_kernel(const uint4 *__res
     const size_t o = (size_t(b) * H + h) * S_pad + i;
     if (i < S_pad) {
       float l2 = __int_as_float(0x7f800000);
+      float xq = -1e30f;
       if (i < S) {
         const float L = lse[(size_t(b) * H + h) * S + i];
-        if (L != -__int_as_float(0x7f800000)) l2 = L * 1.4426950408889634f;
+        if (L != -__int_as_float(0x7f800000)) {
+          l2 = L * 1.4426950408889634f;
+          xq = -L * 11.313708498984761f;   // sqrt(128)
+        }
       }
       delta[o] = mine;
       lse2[o] = l2;
+      qx[o] = bf16_split_row(xq);
+      dox[o] = bf16_split_row(-mine);
     }
   }
 }
@@ -82,14 +107,16 @@ cudaError_t launch_delta(const void *out, const void *dout, const float *lse, co
   char *base = static_cast<char *>(workspace);
   float *delta = reinterpret_cast<float *>(base + w.off_delta);
   float *lse2 = reinterpret_cast<float *>(base + w.off_lse2);
+  uint4 *qx = reinterpret_cast<uint4 *>(base + w.off_qx);
+  uint4 *dox = reinterpret_cast<uint4 *>(base + w.off_dox);
   const int S_pad = w.S_pad;
   const long long tasks = (long long)p.B * ((S_pad + 31) / 32) * p.H;
   long long blocks = (tasks + DELTA_THREADS / 32 - 1) / (DELTA_THREADS / 32);
   const long long cap = (long long)p.num_sms * 8;
   if (blocks > cap) blocks = cap;
   delta_kernel<<<int(blocks), DELTA_THREADS, 0, stream>>>(static_cast<const uint4 *>(out),
-                                                           static_cast<const uint4 *>(dout), lse, delta, lse2, p.B,
-                                                           p.S, p.H, S_pad);
+                                                           static_cast<const uint4 *>(dout), lse, delta, lse2, qx,
+                                                           dox, p.B, p.S, p.H, S_pad);
   return cudaGetLastError();
 }
 
@@ -148,6 +175,8 @@ struct BwArgs {
   const int *list;     // (b * nT + tile), longest first
   const float *delta;  // [B, H, S_pad]
   const float *lse2;   // [B, H, S_pad], lse * log2(e), +inf where nothing is visible
+  const uint4 *qx;     // [B, H, S_pad] offset rows -lse * sqrt(D) (bf16 hi, mid, lo, 0 x 5)
+  const uint4 *dox;    // [B, H, S_pad] offset rows -delta (the same form)
   int *hdr;
   __nv_bfloat16 *out0, *out1;   // dK/dV kernel: dv, dk; dQ kernel: dq
   int B, S, H, nT, S_pad, n_list, n_items;
@@ -185,12 +214,17 @@ __device__ __forceinline__ TileRange dkdv_range(const BwArgs &a, const BwItem &I
 __device__ __forceinline__ int range_tiles(const TileRange &R) { return R.empty() ? 0 : R.last - R.first + 1; }
 
 // ============================================================================= dK/dV
-// Item: (b, h, key tile). Resident: K and V. Streamed: Q_j, dO_j and the rows' lo /
-// lse2 / delta terms (two stages). Per query tile j:
-//   S^T  = K . Q_j^T  -> X           dP^T = V . dO_j^T -> X (after S^T has been read)
-//   P^T  = exp2(S^T c - lse2) (masked)        -> bf16 in PT
+// Item: (b, h, key tile). Resident: K and V. Streamed: Q_j, dO_j, the rows' lo and their
+// two offset rows (two stages). Per query tile j:
+//   X    = K . Q_j^T - lse sqrt(D)  -> X     (dP^T - delta) = V . dO_j^T - delta -> X
+//   P^T  = exp2(X c) (masked)                 -> bf16 in PT
 //   dS^T = P^T (dP^T - delta)                 -> bf16 in DS
 //   dV  += P^T . dO_j,  dK += dS^T . Q_j      (dK scaled by 1/sqrt(D) in the epilogue)
+// The per-query terms are folded into the X products as one more K = 16 slice: a
+// constant block of rows [1, 1, 1, 0, ...] times the query rows' [hi, mid, lo, 0, ...]
+// (the term as three bf16 parts, exact products, fp32 sums), so the softmax warps read
+// no per-query terms from shared memory (that cost about a tenth of the kernel's time).
+// c = log2(e) / sqrt(D); rows that see no key carry -1e30 and give P = 0.
 // TMEM: X [0, 128) fp32, taken by S^T and dP^T in turn | PT [128, 192) | DS [192, 256)
 // (bf16 pairs) | dV [256, 384) | dK [384, 512). The softmax warps read X out first
 // thing in each phase, so the next S^T or dP^T runs while they still work on this one;
@@ -200,10 +234,20 @@ __device__ __forceinline__ int range_tiles(const TileRange &R) { return R.empty(
 // since they then interleave with the next S^T on the tensor core and delay it; and
 // splitting every X product into two 64-query halves, one chain per softmax warpgroup,
 // 13 %.)
-constexpr int KV_STAGE_BYTES = 2 * TILE_BYTES + 3 * RT_BYTES;   // Q, dO, lo, lse2, delta
+// stage: Q, dO (128B-swizzled tiles), lo (int32), the offset rows of -lse sqrt(D) and of
+// -delta (128 x 16 bytes each: core matrices of 8 rows, 128 bytes apart)
+constexpr int KV_OFF_LO = 2 * TILE_BYTES;
+constexpr int KV_OFF_QX = KV_OFF_LO + RT_BYTES;
+constexpr int KV_OFF_DOX = KV_OFF_QX + BM * XROW_BYTES;
+constexpr int KV_STAGE_BYTES = KV_OFF_DOX + BM * XROW_BYTES;
 constexpr int KV_STAGE_STRIDE = (KV_STAGE_BYTES + 1023) & ~1023;
-constexpr int KVB_SM_K = 0, KVB_SM_V = TILE_BYTES, KVB_SM_ST = 2 * TILE_BYTES;
+// the constant operand of the folded slice: 128 rows of [1, 1, 1, 0 x 5] (K elements
+// 0-7), then 128 rows of zeros (K elements 8-15)
+constexpr int KV_ONES_BYTES = 2 * BN * XROW_BYTES;
+constexpr int KVB_SM_K = 0, KVB_SM_V = TILE_BYTES, KVB_SM_ONES = 2 * TILE_BYTES;
+constexpr int KVB_SM_ST = KVB_SM_ONES + KV_ONES_BYTES;
 constexpr int KVB_SM_BAR = KVB_SM_ST + 2 * KV_STAGE_STRIDE;
+static_assert(KVB_SM_ST % 1024 == 0, "128B-swizzled tiles start on 1024-byte boundaries");
 constexpr uint32_t KV_COL_X = 0, KV_COL_PT = 128, KV_COL_DS = 192, KV_COL_DV = 256, KV_COL_DK = 384;
 
 struct KvbBars {
@@ -255,9 +299,9 @@ __device__ __forceinline__ bool kv_producer(const CUtensorMap *tq, const CUtenso
       const int row0 = (R.first + j) * BM;
       load_tile(tq, &bars->st_full[st], dst, I.h, row0, I.b);
       load_tile(tdo, &bars->st_full[st], dst + TILE_BYTES, I.h, row0, I.b);
-      bulk_load(dst + 2 * TILE_BYTES, a.lo + size_t(I.b) * a.S_pad + row0, RT_BYTES, &bars->st_full[st]);
-      bulk_load(dst + 2 * TILE_BYTES + RT_BYTES, a.lse2 + rowbase + row0, RT_BYTES, &bars->st_full[st]);
-      bulk_load(dst + 2 * TILE_BYTES + 2 * RT_BYTES, a.delta + rowbase + row0, RT_BYTES, &bars->st_full[st]);
+      bulk_load(dst + KV_OFF_LO, a.lo + size_t(I.b) * a.S_pad + row0, RT_BYTES, &bars->st_full[st]);
+      bulk_load(dst + KV_OFF_QX, a.qx + rowbase + row0, BM * XROW_BYTES, &bars->st_full[st]);
+      bulk_load(dst + KV_OFF_DOX, a.dox + rowbase + row0, BM * XROW_BYTES, &bars->st_full[st]);
       ++fill;
     }
     if (!ok) break;
@@ -270,21 +314,25 @@ __device__ __forceinline__ bool kv_producer(const CUtensorMap *tq, const CUtenso
   return ok;
 }
 
-// Issuer of the X products: S^T(j) = K Q_j^T then dP^T(j) = V dO_j^T, each once the
-// softmax warps have read the previous X product out (x_free). Releases K and V after
-// the item's last product.
+// Issuer of the X products: S^T(j) - lse sqrt(D) = K Q_j^T + ones qx_j^T, then
+// dP^T(j) - delta = V dO_j^T + ones dox_j^T, each once the softmax warps have read the
+// previous X product out (x_free). Releases K and V after the item's last product.
 __device__ __forceinline__ bool kv_x_issuer(const BwArgs &a, uint8_t *smem, KvbBars *bars, uint32_t tmem, int lane) {
   WaitCtl *abort = &bars->ctl;
   const uint32_t k_s = smem_u32(smem + KVB_SM_K), v_s = smem_u32(smem + KVB_SM_V);
   const uint32_t st0 = smem_u32(smem + KVB_SM_ST);
+  // ones: K elements 8-15 are the zero rows behind the 128 rows of ones; the offset rows'
+  // K elements 8-15 re-read elements 0-7 (lbo 0), which the zeros cancel exactly
+  const uint64_t ones_desc = sdesc_plain(smem_u32(smem + KVB_SM_ONES), BN * XROW_BYTES, 8 * XROW_BYTES);
   int use = 0, own = 0, n_x = 0;
   int seen = 0;   // stages whose arrival this warp has observed (the abort path waits for the rest)
   bool ok = true;
-  auto x_product = [&](uint32_t a_s, uint32_t b_s, uint64_t *done) -> bool {
+  auto x_product = [&](uint32_t a_s, uint32_t b_s, uint32_t off_s, uint64_t *done) -> bool {
     if (n_x > 0 && !mbar_wait(&bars->x_free, (n_x - 1) & 1, abort)) return false;
     tc_fence_after();
     if (lane == 0) {
-      mma_tile_kk(tmem + KV_COL_X, a_s, b_s, false);
+      mma_ss(tmem + KV_COL_X, ones_desc, sdesc_plain(off_s, 0, 8 * XROW_BYTES), IDESC_128_KK, 0u);
+      mma_tile_kk(tmem + KV_COL_X, a_s, b_s, true);
       mma_commit(done);
     }
     __syncwarp();
@@ -307,8 +355,8 @@ __device__ __forceinline__ bool kv_x_issuer(const BwArgs &a, uint8_t *smem, KvbB
       if (!(ok = mbar_wait(&bars->st_full[k & 1], (k >> 1) & 1, abort))) break;
       seen = k + 1;
       const uint32_t q_s = st0 + uint32_t(k & 1) * KV_STAGE_STRIDE;
-      if (!(ok = x_product(k_s, q_s, &bars->s_full))) break;               // S^T(j)
-      if (!(ok = x_product(v_s, q_s + TILE_BYTES, &bars->dp_full))) break;  // dP^T(j)
+      if (!(ok = x_product(k_s, q_s, q_s + KV_OFF_QX, &bars->s_full))) break;                 // S^T(j)
+      if (!(ok = x_product(v_s, q_s + TILE_BYTES, q_s + KV_OFF_DOX, &bars->dp_full))) break;  // dP^T(j)
     }
     if (!ok) break;
     use += n;
@@ -323,8 +371,9 @@ __device__ __forceinline__ bool kv_x_issuer(const BwArgs &a, uint8_t *smem, KvbB
 }
 
 // Issuer of the accumulating products: dV += P^T(j) dO_j once P^T is written, dK +=
-// dS^T(j) Q_j once dS^T is written; then releases the stage (its row terms were read
-// before dS^T was signalled). The first products of an item overwrite dV and dK once
+// dS^T(j) Q_j once dS^T is written; then releases the stage (its lo terms were read,
+// and the X products that read its offset rows had completed, before dS^T was
+// signalled). The first products of an item overwrite dV and dK once
 // the previous item's have been read out.
 __device__ __forceinline__ bool kv_acc_issuer(const BwArgs &a, uint8_t *smem, KvbBars *bars, uint32_t tmem,
                                               int lane) {
@@ -405,15 +454,13 @@ __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBa
     for (int j = 0; j < n; ++j, ++use, ++n_done) {
       const int st = use & 1;
       const uint8_t *stage = smem + KVB_SM_ST + st * KV_STAGE_STRIDE;
-      const int *lo_q = reinterpret_cast<const int *>(stage + 2 * TILE_BYTES);
-      const float4 *l2_q = reinterpret_cast<const float4 *>(stage + 2 * TILE_BYTES + RT_BYTES) + 16 * w;
-      const float4 *dl_q = reinterpret_cast<const float4 *>(stage + 2 * TILE_BYTES + 2 * RT_BYTES) + 16 * w;
+      const int *lo_q = reinterpret_cast<const int *>(stage + KV_OFF_LO);
       const int q0 = (R.first + j) * BM;
 
       // ---- P phase
       if (!(ok = mbar_wait(&bars->s_full, sf_par, abort))) break;
       sf_par ^= 1;
-      // the stage's row terms arrived by bulk copy: observe the stage's barrier
+      // the stage's lo terms arrived by bulk copy: observe the stage's barrier
       if (!(ok = mbar_wait(&bars->st_full[st], (use >> 1) & 1, abort))) break;
       tc_fence_after();
       float p[64];
@@ -444,12 +491,7 @@ __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBa
       q_from -= 64 * w;
       q_to -= 64 * w;
 #pragma unroll
-      for (int e4 = 0; e4 < 16; ++e4) {
-        const float4 l2 = l2_q[e4];
-        const float l2v[4] = {l2.x, l2.y, l2.z, l2.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) p[e4 * 4 + e] = ex2_approx(fmaf(p[e4 * 4 + e], c, -l2v[e]));
-      }
+      for (int e = 0; e < 64; ++e) p[e] = ex2_approx(p[e] * c);
       if (!full) {
 #pragma unroll
         for (int q = 0; q < 64; ++q)
@@ -486,17 +528,8 @@ __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBa
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->x_free);   // dP^T is in registers: X may take S^T(j+1)
 #pragma unroll
-        for (int e4 = 0; e4 < 16; e4 += 2) {
-          const float4 d0 = dl_q[e4], d1 = dl_q[e4 + 1];
-          const float dlv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int q = e4 * 4 + e;
-            const float s0 = p[q] * (__uint_as_float(dv[q]) - dlv[e]);
-            const float s1 = p[q + 1] * (__uint_as_float(dv[q + 1]) - dlv[e + 1]);
-            dk[q / 2] = pack_bf16x2(s0, s1);
-          }
-        }
+        for (int e = 0; e < 32; ++e)
+          dk[e] = pack_bf16x2(p[2 * e] * __uint_as_float(dv[2 * e]), p[2 * e + 1] * __uint_as_float(dv[2 * e + 1]));
       }
       // DS belongs to the previous dK product until it completes
       if (n_done > 0) {
@@ -564,6 +597,12 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     bars->ctl.init(a.wait);
     bars->fill = bars->use = bars->own_issued = bars->own_used = 0;
     fence_mbar_init();
+  }
+  if (threadIdx.x < KV_ONES_BYTES / 16) {   // the folded slice's constant operand
+    const uint32_t one = 0x3F80u;           // bf16 1.0
+    reinterpret_cast<uint4 *>(smem + KVB_SM_ONES)[threadIdx.x] =
+        threadIdx.x < BN ? make_uint4(one | (one << 16), one, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
   }
   if (warp == BW_MMA) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -1025,6 +1064,8 @@ BwArgs bw_args(const Problem &p, void *workspace, const int *list) {
   a.list = list;
   a.delta = reinterpret_cast<const float *>(base + w.off_delta);
   a.lse2 = reinterpret_cast<const float *>(base + w.off_lse2);
+  a.qx = reinterpret_cast<const uint4 *>(base + w.off_qx);
+  a.dox = reinterpret_cast<const uint4 *>(base + w.off_dox);
   a.hdr = reinterpret_cast<int *>(base + w.off_hdr);
   a.out0 = a.out1 = nullptr;
   a.B = p.B;

@@ -44,8 +44,11 @@ enum HeaderWord {
   HDR_WORDS = 64
 };
 
+constexpr int XROW_BYTES = 16;     // one bf16 offset row of the dK/dV kernel (see Workspace)
+
 struct Workspace {
-  size_t off_hdr, off_lo, off_kend, off_list_fwd, off_list_kv, off_list_q, off_delta, off_lse2, off_dqacc, total;
+  size_t off_hdr, off_lo, off_kend, off_list_fwd, off_list_kv, off_list_q, off_delta, off_lse2, off_qx, off_dox,
+      off_dqacc, total;
   size_t dqacc_bytes;
   int nT, nP, S_pad;   // S_pad = nT * BM: per-row stride of lo, delta and lse2
 
@@ -66,6 +69,10 @@ struct Workspace {
     // backward row terms, fp32 [B, H, nT * BM] (rows padded to whole tiles)
     w.off_delta = o;    o += align256(size_t(B) * H * w.S_pad * 4);
     w.off_lse2 = o;     o += align256(size_t(B) * H * w.S_pad * 4);
+    // the same two row terms as the dK/dV kernel's offset rows, bf16 [B, H, S_pad, 8]:
+    // -lse * sqrt(D) and -delta, each as hi + mid + lo (see delta_kernel)
+    w.off_qx = o;       o += align256(size_t(B) * H * w.S_pad * XROW_BYTES);
+    w.off_dox = o;      o += align256(size_t(B) * H * w.S_pad * XROW_BYTES);
     // fp32 dQ accumulator of the single-kernel backward pass, [B, H, S_pad, D]
     w.dqacc_bytes = size_t(B) * H * w.S_pad * HD * 4;
     w.off_dqacc = o;    o += align256(w.dqacc_bytes);
@@ -292,6 +299,23 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   d |= uint64_t(1) << 46;
   d |= uint64_t(2) << 61;
   return d;
+}
+
+// The same descriptor for a K-major operand stored without swizzle: core matrices of
+// 8 rows x 16 bytes (128 contiguous bytes); lbo = byte offset between the two core
+// matrices along K (a K = 16 bf16 slice), sbo = byte offset between 8-row groups.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t(1) << 46;
+  return d;
+}
+
+// Makes this thread's shared-memory stores visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Instruction descriptor for kind::f16 with bf16 inputs and an fp32 accumulator.

@@ -16,6 +16,8 @@
 // once in shared memory by a bulk copy (an online max / sum pass and the gradient pass
 // both read it there); beyond that, one warp per row reading the logits twice. The loss
 // is summed per CTA and the CTA sums in a fixed order: deterministic for a given input.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(CE_WARPS * 32) ce_kernel(const __grid_constant
 // read once (the warp-per-row kernel above re-reads its row, from HBM once the rows in
 // flight outgrow L2).
 constexpr int CE_ROW_THREADS = 256;
-constexpr int CE_ROW_MAX_BYTES = 96 * 1024;   // two CTAs per SM
+constexpr int CE_ROW_MAX_BYTES = 96 * 1024;   // at least two CTAs per SM
 
 __device__ __forceinline__ float block_sum_256(float v, float *red) {
   for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
@@ -242,7 +244,7 @@ __device__ __forceinline__ float block_max_256(float v, float *red) {
   return t;
 }
 
-__global__ void __launch_bounds__(CE_ROW_THREADS, 2) ce_row_kernel(const __grid_constant__ CeArgs a) {
+__global__ void __launch_bounds__(CE_ROW_THREADS, 3) ce_row_kernel(const __grid_constant__ CeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint4 *row = reinterpret_cast<uint4 *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   __shared__ uint64_t full;
@@ -415,10 +417,14 @@ cudaError_t launch_packed_loss(const void *logits, const int *targets, const flo
   int n_part = l.n_cta;
   if (V * 2 <= CE_ROW_MAX_BYTES) {
     static std::atomic<uint64_t> attr_done{0};
-    const int smem = CE_ROW_MAX_BYTES + 128;
-    if ((e = smem_attr_once(reinterpret_cast<const void *>(ce_row_kernel), smem, attr_done)) != cudaSuccess) return e;
+    // the row buffer decides how many CTAs share an SM (up to 3: one loads while others compute)
+    const int smem = V * 2 + 128;
+    if ((e = smem_attr_once(reinterpret_cast<const void *>(ce_row_kernel), CE_ROW_MAX_BYTES + 128, attr_done)) !=
+        cudaSuccess)
+      return e;
+    const int per_sm = std::max(1, std::min(3, (227 * 1024) / (smem + 1024)));
     const long long rows = (long long)B * S;
-    long long grid = (long long)num_sms * 2;
+    long long grid = (long long)num_sms * per_sm;
     if (grid > rows) grid = rows;
     if (grid > l.n_cta) grid = l.n_cta;
     n_part = int(grid);

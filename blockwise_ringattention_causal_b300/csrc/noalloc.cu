@@ -57,9 +57,9 @@ extern "C" lwm_status lwm_attn_fwd_noalloc(const lwm_bf16 *q, const lwm_bf16 *k,
   const lwm_status sz = check_sizes(B, S, H, D);
   if (sz != LWM_OK) return sz;
   // The forward pass uses only the part of the workspace in front of the backward
-  // rows; its size does not depend on H, and the layout with H = 1 (without the dQ
-  // accumulator of the backward pass) covers it.
-  if (Workspace::layout(B, S, 1).off_dqacc > NOALLOC_BYTES) return LWM_ERR_INVALID_ARG;
+  // rows; its size does not depend on H, and the layout with H = 1 up to the dK/dV
+  // kernel's offset rows covers it.
+  if (Workspace::layout(B, S, 1).off_qx > NOALLOC_BYTES) return LWM_ERR_INVALID_ARG;
   if (!q || !k || !v || !out || !lse) return LWM_ERR_INVALID_ARG;
   const auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   const auto a4 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
