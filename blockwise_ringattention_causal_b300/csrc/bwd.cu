@@ -664,28 +664,31 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 // ============================================================================= dQ
 // Item: (b, h, query tile). Resident: Q and dO; the rows' lo / lse2 / delta live in
 // registers (thread = query row). Streamed: K_j (ring of three) and V_j (ring of two).
-// Per key tile j:
-//   S    = Q . K_j^T  -> A_{j % 2}      dP = dO . V_j^T -> B
-//   P    = exp2(S c - lse2) (masked),  dS = P (dP - delta)  -> bf16 over A_{j % 2}
-//   dQ  += dS . K_j   (C; scaled by 1/sqrt(D) in the epilogue)
-// TMEM: A0 [0, 128), A1 [128, 256), B [256, 384), C [384, 512). Three MMA issuers: warp
-// 9 runs dQ(j), warp 10 dP(j), warp 11 S(j) (up to two tiles ahead). Deterministic: every
-// dQ row is summed by one CTA in a fixed order.
+// Per key tile g (counted over all items of the CTA):
+//   S    = Q . K_g^T  -> X                 dP = dO . V_g^T -> Y_{g % 2}
+//   P    = exp2(S c - lse2) (masked),  dS = P (dP - delta)  -> bf16 over its own dP
+//   dQ  += dS . K_g   (C; scaled by 1/sqrt(D) in the epilogue)
+// TMEM: X [0, 128), Y0 [128, 256), Y1 [256, 384), C [384, 512). X is free as soon as the
+// softmax warps have read S out, so S(g + 1) runs while they work on tile g; the dP
+// products are double-buffered, so dP(g + 1) runs before the dS phase of g ends (it
+// waits only for dQ(g - 1), the last reader of its slot). Three MMA issuers: warp 9 runs
+// dQ(g), warp 10 dP(g), warp 11 S(g). Deterministic: every dQ row is summed by one CTA
+// in a fixed order.
 constexpr int DQ_KSTAGES = 3, DQ_VSTAGES = 2;
 constexpr int DQ_SM_Q = 0, DQ_SM_DO = TILE_BYTES, DQ_SM_K = 2 * TILE_BYTES;
 constexpr int DQ_SM_V = DQ_SM_K + DQ_KSTAGES * TILE_BYTES;
 constexpr int DQ_SM_BAR = DQ_SM_V + DQ_VSTAGES * TILE_BYTES;
-constexpr uint32_t DQ_COL_B = 256, DQ_COL_C = 384;
+constexpr uint32_t DQ_COL_X = 0, DQ_COL_Y = 128, DQ_COL_C = 384;
 
 struct DqBars {
   uint64_t k_full[DQ_KSTAGES], k_empty[DQ_KSTAGES], v_full[DQ_VSTAGES], v_empty[DQ_VSTAGES];
   uint64_t own_full, own_empty;
-  // dS(j) written: ds_full[j % 2] is waited by chain 0 (slot A_{j % 2}), ds_dp by chain 1.
-  // One barrier per slot: chain 0 issues S(j + 2) only after its wait for dS(j), so the
-  // softmax cannot complete a second phase of that slot's barrier before the wait (a
-  // single barrier could run two phases ahead and alias the parity).
-  uint64_t s_full[2], dp_full, ds_full[2], ds_dp;
-  uint64_t a_free[2];   // dQ(j) has completed: slot A_{j % 2} may take S(j + 2)
+  uint64_t s_full, x_free;   // S(g) written to X; the softmax warps have read it out
+  // slot Y_{g % 2}: dP(g) written; dS(g) written over it; dQ(g), its last reader, done.
+  // Every waiter's next phase on one of them needs an action the waiter takes after its
+  // wait (S(g + 1) after x_free(g), dP(g + 2) after y_free(g), dQ(g) after ds_full(g)),
+  // so no barrier can run two phases ahead of its waiter.
+  uint64_t dp_full[2], ds_full[2], y_free[2];
   uint64_t acc_full, acc_empty;
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
@@ -747,21 +750,20 @@ __device__ __forceinline__ bool dq_producer(const CUtensorMap *tq, const CUtenso
   return ok;
 }
 
-// MMA chains of the dQ kernel, one issuing warp each:
-//   chain 0 (warp 9):  dQ += dS(j) K_j once the softmax has written dS(j) over A_{j % 2};
-//                      then releases K_j and the slot A_{j % 2} (a_free, on completion);
-//   chain 1 (warp 10): dP(j) = dO V_j^T into B, after the softmax read the previous dP;
-//   chain 2 (warp 11): S(j) = Q K_j^T into A_{j % 2}, once the dQ product that last read
-//                      that slot has completed (it runs up to two tiles ahead).
+// MMA chains of the dQ kernel, one issuing warp each (g = the CTA's running key-tile
+// count, slot s = g % 2):
+//   chain 0 (warp 9):  dQ += dS(g) K_g once the softmax has written dS(g) over Y_s; then
+//                      releases K_g and Y_s (on completion);
+//   chain 1 (warp 10): dP(g) = dO V_g^T into Y_s once dQ(g - 2) has released it;
+//   chain 2 (warp 11): S(g) = Q K_g^T into X once the softmax has read S(g - 1) out.
 __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *bars, uint32_t tmem, int chain,
                                        int lane) {
   WaitCtl *abort = &bars->ctl;
   const uint32_t q_s = smem_u32(smem + DQ_SM_Q), do_s = smem_u32(smem + DQ_SM_DO);
   const uint32_t k0_s = smem_u32(smem + DQ_SM_K), v0_s = smem_u32(smem + DQ_SM_V);
-  int k_use = 0, v_use = 0, own = 0, dp_issued = 0;
-  int k_seen = 0;               // K stages whose arrival chain 2 has observed (the abort path waits for the rest)
-  int a_uses[2] = {0, 0};       // S products written into each A slot so far (chain 2)
-  uint32_t dsf_par[2] = {0, 0}, dsp_par = 0, ae_par = 1;
+  int k_use = 0, v_use = 0, own = 0, g = 0;
+  int k_seen = 0;   // K stages whose arrival chain 2 has observed (the abort path waits for the rest)
+  uint32_t ae_par = 1;
   bool ok = true;
   for (int it = 0; ok; ++it) {
     const int slot = it & 1;
@@ -781,20 +783,20 @@ __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *b
     auto k_par = [&](int j) { return uint32_t((kb + j) / DQ_KSTAGES) & 1u; };
     if (chain == 0) {
       for (int j = 0; j < n && ok; ++j) {
-        if (!(ok = mbar_wait(&bars->ds_full[j & 1], dsf_par[j & 1], abort))) break;
-        dsf_par[j & 1] ^= 1;
+        const int gg = g + j, s = gg & 1;
+        if (!(ok = mbar_wait(&bars->ds_full[s], uint32_t(gg >> 1) & 1u, abort))) break;
         if (j == 0) {
           if (!(ok = mbar_wait(&bars->acc_empty, ae_par, abort))) break;
           ae_par ^= 1;
         }
-        // K_j arrived (chain 2 saw it before S(j)); the stage stays until this chain releases it
+        // K_g arrived (chain 2 saw it before S(g)); the stage stays until this chain releases it
         if (!(ok = mbar_wait(&bars->k_full[k_stage(j)], k_par(j), abort))) break;
         tc_fence_after();
         if (lane == 0) {
-          mma_tile_ts(tmem + DQ_COL_C, tmem + uint32_t(j & 1) * 128,
+          mma_tile_ts(tmem + DQ_COL_C, tmem + DQ_COL_Y + uint32_t(s) * 128,
                       k0_s + uint32_t(k_stage(j)) * TILE_BYTES, j > 0);   // dQ += dS K
           mma_commit(&bars->k_empty[k_stage(j)]);
-          mma_commit(&bars->a_free[j & 1]);
+          mma_commit(&bars->y_free[s]);
         }
         __syncwarp();
       }
@@ -803,39 +805,37 @@ __device__ __forceinline__ bool dq_mma(const BwArgs &a, uint8_t *smem, DqBars *b
       __syncwarp();
     } else if (chain == 2) {
       for (int j = 0; j < n && ok; ++j) {
+        const int gg = g + j;
         if (!(ok = mbar_wait(&bars->k_full[k_stage(j)], k_par(j), abort))) break;
         k_seen = kb + j + 1;
-        const int s = j & 1;
-        if (a_uses[s] > 0 && !(ok = mbar_wait(&bars->a_free[s], uint32_t(a_uses[s] - 1) & 1u, abort))) break;
-        ++a_uses[s];
+        if (gg > 0 && !(ok = mbar_wait(&bars->x_free, uint32_t(gg - 1) & 1u, abort))) break;
         tc_fence_after();
         if (lane == 0) {
-          mma_tile_kk(tmem + uint32_t(s) * 128, q_s, k0_s + uint32_t(k_stage(j)) * TILE_BYTES, false);   // S = Q K^T
-          mma_commit(&bars->s_full[s]);
+          mma_tile_kk(tmem + DQ_COL_X, q_s, k0_s + uint32_t(k_stage(j)) * TILE_BYTES, false);   // S = Q K^T
+          mma_commit(&bars->s_full);
         }
         __syncwarp();
       }
       if (!ok) break;
     } else {
       for (int j = 0; j < n && ok; ++j, ++v_use) {
+        const int gg = g + j, s = gg & 1;
         const int vs = v_use % DQ_VSTAGES;
         if (!(ok = mbar_wait(&bars->v_full[vs], (v_use / DQ_VSTAGES) & 1, abort))) break;
-        if (dp_issued > 0) {   // B still holds the previous dP until its dS phase is done
-          if (!(ok = mbar_wait(&bars->ds_dp, dsp_par, abort))) break;
-          dsp_par ^= 1;
-        }
+        if (gg >= 2 && !(ok = mbar_wait(&bars->y_free[s], uint32_t((gg - 2) >> 1) & 1u, abort))) break;
         tc_fence_after();
         if (lane == 0) {
-          mma_tile_kk(tmem + DQ_COL_B, do_s, v0_s + uint32_t(vs) * TILE_BYTES, false);   // dP = dO V^T
-          mma_commit(&bars->dp_full);
+          mma_tile_kk(tmem + DQ_COL_Y + uint32_t(s) * 128, do_s, v0_s + uint32_t(vs) * TILE_BYTES,
+                      false);   // dP = dO V^T
+          mma_commit(&bars->dp_full[s]);
           mma_commit(&bars->v_empty[vs]);
         }
         __syncwarp();
-        ++dp_issued;
       }
       if (!ok) break;
     }
     k_use = kb + n;
+    g += n;
     if (chain != 0) {
       if (lane == 0) mma_commit(&bars->own_empty);
       __syncwarp();
@@ -856,9 +856,10 @@ __device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
   const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-  const uint32_t tB = tmem + lane_off + DQ_COL_B + 64 * w;
+  const uint32_t tX = tmem + lane_off + DQ_COL_X + 64 * w;
   const float c = a.scale_log2;
-  uint32_t sf_par[2] = {0, 0}, dpf_par = 0, af_par = 0;
+  uint32_t af_par = 0;
+  int g = 0;
   bool ok = true;
   for (int it = 0; ok; ++it) {
     const int slot = it & 1;
@@ -876,55 +877,50 @@ __device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32
     const int lo_i = lr[i];
     const int lo_last = lr[q0 + BM - 1];
     const float l2 = a.lse2[rowterm], dl = a.delta[rowterm];
-    for (int j = 0; j < n; ++j) {
+    for (int j = 0; j < n; ++j, ++g) {
       const int k0 = (R.first + j) * BN;
-      const uint32_t tA = tmem + lane_off + uint32_t(j & 1) * 128 + 64 * w;
+      const uint32_t tY = tmem + lane_off + DQ_COL_Y + uint32_t(g & 1) * 128 + 64 * w;
       const bool full = lo_last <= k0 && k0 + BN - 1 <= q0;
       // visible keys of query i: lo_i <= key <= i, i.e. columns [c_from, c_to) here
       const int c_from = lo_i - k0 - 64 * w, c_to = i - k0 - 64 * w + 1;
 
-      // ---- P phase
-      if (!(ok = mbar_wait(&bars->s_full[j & 1], sf_par[j & 1], abort))) break;
-      sf_par[j & 1] ^= 1;
+      // ---- P phase: read S out of X (which then takes S(g + 1)), P in registers
+      if (!(ok = mbar_wait(&bars->s_full, uint32_t(g) & 1u, abort))) break;
       tc_fence_after();
       float p[64];
-      uint32_t sv[64];
-      tmem_ld16(tA, sv);
-      tmem_ld16(tA + 16, sv + 16);
+      {
+        uint32_t sv[64];
+        tmem_ld16(tX, sv);
+        tmem_ld16(tX + 16, sv + 16);
+        tmem_ld16(tX + 32, sv + 32);
+        tmem_ld16(tX + 48, sv + 48);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->x_free);
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        if (ch == 0 || ch == 2) {
-          tmem_ld_wait();
-          if (ch == 0) {
-            tmem_ld16(tA + 32, sv + 32);
-            tmem_ld16(tA + 48, sv + 48);
-          }
-        }
+        for (int e = 0; e < 64; ++e) p[e] = ex2_approx(fmaf(__uint_as_float(sv[e]), c, -l2));
+      }
+      if (!full) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) p[ch * 16 + e] = ex2_approx(fmaf(__uint_as_float(sv[ch * 16 + e]), c, -l2));
-        if (!full) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int cc = ch * 16 + e;
-            if (cc < c_from || cc >= c_to) p[cc] = 0.f;
-          }
-        }
+        for (int cc = 0; cc < 64; ++cc)
+          if (cc < c_from || cc >= c_to) p[cc] = 0.f;
       }
 
-      // ---- dS phase
-      if (!(ok = mbar_wait(&bars->dp_full, dpf_par, abort))) break;
-      dpf_par ^= 1;
+      // ---- dS phase: dS over the dP columns just read (each 16-column block's first 8
+      // columns take its 16 bf16 values; no block is written before it has been read)
+      if (!(ok = mbar_wait(&bars->dp_full[g & 1], uint32_t(g >> 1) & 1u, abort))) break;
       tc_fence_after();
       uint32_t dv[64];
-      tmem_ld16(tB, dv);
-      tmem_ld16(tB + 16, dv + 16);
+      tmem_ld16(tY, dv);
+      tmem_ld16(tY + 16, dv + 16);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         if (ch == 0 || ch == 2) {
           tmem_ld_wait();
           if (ch == 0) {
-            tmem_ld16(tB + 32, dv + 32);
-            tmem_ld16(tB + 48, dv + 48);
+            tmem_ld16(tY + 32, dv + 32);
+            tmem_ld16(tY + 48, dv + 48);
           }
         }
         uint32_t dk[8];
@@ -932,15 +928,12 @@ __device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32
         for (int e = 0; e < 8; ++e)
           dk[e] = pack_bf16x2(p[ch * 16 + 2 * e] * (__uint_as_float(dv[ch * 16 + 2 * e]) - dl),
                               p[ch * 16 + 2 * e + 1] * (__uint_as_float(dv[ch * 16 + 2 * e + 1]) - dl));
-        tmem_st8(tA + ch * 16, dk);
+        tmem_st8(tY + ch * 16, dk);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars->ds_full[j & 1]);
-        mbar_arrive(&bars->ds_dp);
-      }
+      if (lane == 0) mbar_arrive(&bars->ds_full[g & 1]);
     }
     if (!ok) break;
 
@@ -979,16 +972,16 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       mbar_init(&bars->v_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->dp_full[s], 1);
       mbar_init(&bars->ds_full[s], 8);
-      mbar_init(&bars->a_free[s], 1);
+      mbar_init(&bars->y_free[s], 1);
       mbar_init(&bars->item_full[s], 1);
       mbar_init(&bars->item_empty[s], 11);  // softmax 8 + MMA 3 warps
     }
     mbar_init(&bars->own_full, 1);
     mbar_init(&bars->own_empty, 2);
-    mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->ds_dp, 8);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->x_free, 8);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 3);
