@@ -313,6 +313,21 @@ __device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// Register reconfiguration of a whole warpgroup (all four warps execute the same one).
+// A shrink returns registers to the CTA's pool at once; a grow waits until the pool
+// holds them, so the grows of a kernel must fit what its shrinks release plus what the
+// launch left unused.
+template <int N>
+__device__ __forceinline__ void reg_shrink() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_grow() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Makes this thread's shared-memory stores visible to the tensor core (async proxy).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -28,13 +28,21 @@
 namespace lwm {
 namespace {
 
-constexpr int FWD_WARPS = 12;   // 3 warps per SM sub-partition: 168 registers each
+constexpr int FWD_WARPS = 12;   // 3 warps per SM sub-partition: 168 registers each at launch
 constexpr int FWD_THREADS = FWD_WARPS * 32;
 constexpr int WARP_PRODUCER = 8;
 constexpr int WARP_MMA = 9;    // issuer of the S products (and TMEM owner)
 constexpr int WARP_PV0 = 10;   // issuers of the P.V products of query tiles 0 and 1
 constexpr int WARP_PV1 = 11;
 constexpr int KV_STAGES = 4;
+// Register split (setmaxnreg): the block is launched with 168 registers per thread
+// (384 threads, 64,512 in all); warpgroup 2 (producer and issuers) shrinks to
+// FWD_REGS_OTHER and the two softmax warpgroups grow to FWD_REGS_SOFTMAX:
+// 2 x 128 x 200 + 128 x 96 = 63,488 <= 64,512. At 168 the softmax, which holds a
+// 128-column score row per thread, spilled about 11 values per warp and tile.
+constexpr int FWD_REGS_SOFTMAX = 200, FWD_REGS_OTHER = 96;
+static_assert(2 * 128 * FWD_REGS_SOFTMAX + 128 * FWD_REGS_OTHER <= 168 * FWD_THREADS,
+              "register split must fit the launch's registers");
 static_assert(KV_STAGES % 2 == 0, "K tiles take the even stages, V tiles the odd ones");
 
 constexpr int SM_Q = 0;
@@ -515,14 +523,18 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   const uint32_t tmem = bars->tmem_base;
 
   bool ok = true;
-  if (warp == WARP_PRODUCER) {
-    if (lane == 0) ok = producer_role<TEST>(&tq, &tk, &tv, a, smem, bars, kv_chunk);
-    __syncwarp();
-  } else if (warp == WARP_MMA) {
-    ok = s_issuer_role(a, smem, bars, tmem, kv_chunk, lane);
-  } else if (warp == WARP_PV0 || warp == WARP_PV1) {
-    ok = pv_issuer_role(a, smem, bars, tmem, kv_chunk, warp - WARP_PV0, lane);
-  } else if (warp < 8) {
+  if (warp >= WARP_PRODUCER) {   // warpgroup 2: producer and MMA issuers, few registers each
+    reg_shrink<FWD_REGS_OTHER>();
+    if (warp == WARP_PRODUCER) {
+      if (lane == 0) ok = producer_role<TEST>(&tq, &tk, &tv, a, smem, bars, kv_chunk);
+      __syncwarp();
+    } else if (warp == WARP_MMA) {
+      ok = s_issuer_role(a, smem, bars, tmem, kv_chunk, lane);
+    } else {
+      ok = pv_issuer_role(a, smem, bars, tmem, kv_chunk, warp - WARP_PV0, lane);
+    }
+  } else {   // warpgroups 0, 1: softmax, a full 128-column score row per thread
+    reg_grow<FWD_REGS_SOFTMAX>();
     ok = softmax_role(a, bars, tmem, kv_chunk, warp >> 2, warp, lane);
   }
   if (!ok) {
