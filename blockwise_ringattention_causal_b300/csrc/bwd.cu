@@ -436,7 +436,7 @@ __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBa
   const uint32_t tX = tmem + lane_off + KV_COL_X + 64 * w;
   const uint32_t tPT = tmem + lane_off + KV_COL_PT + 32 * w;
   const uint32_t tDS = tmem + lane_off + KV_COL_DS + 32 * w;
-  const float c = a.scale_log2;
+  const uint64_t c2 = f2_pack(a.scale_log2, a.scale_log2);
   uint32_t sf_par = 0, dpf_par = 0, af_par = 0;
   int use = 0, n_done = 0;   // n_done: query tiles finished (all items), = dV / dK products issued before
   bool ok = true;
@@ -491,7 +491,12 @@ __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBa
       q_from -= 64 * w;
       q_to -= 64 * w;
 #pragma unroll
-      for (int e = 0; e < 64; ++e) p[e] = ex2_approx(p[e] * c);
+      for (int e = 0; e < 64; e += 2) {
+        float x0, x1;
+        f2_unpack(f2_mul(f2_pack(p[e], p[e + 1]), c2), x0, x1);
+        p[e] = ex2_approx(x0);
+        p[e + 1] = ex2_approx(x1);
+      }
       if (!full) {
 #pragma unroll
         for (int q = 0; q < 64; ++q)
@@ -529,7 +534,12 @@ __device__ __forceinline__ bool kv_softmax(const BwArgs &a, uint8_t *smem, KvbBa
         if (lane == 0) mbar_arrive(&bars->x_free);   // dP^T is in registers: X may take S^T(j+1)
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          dk[e] = pack_bf16x2(p[2 * e] * __uint_as_float(dv[2 * e]), p[2 * e + 1] * __uint_as_float(dv[2 * e + 1]));
+        {
+          float s0, s1;
+          f2_unpack(f2_mul(f2_pack(p[2 * e], p[2 * e + 1]),
+                           f2_pack(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1]))), s0, s1);
+          dk[e] = pack_bf16x2(s0, s1);
+        }
       }
       // DS belongs to the previous dK product until it completes
       if (n_done > 0) {
@@ -857,7 +867,7 @@ __device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32
   const int row = quarter * 32 + lane;
   const uint32_t lane_off = uint32_t(quarter * 32) << 16;
   const uint32_t tX = tmem + lane_off + DQ_COL_X + 64 * w;
-  const float c = a.scale_log2;
+  const uint64_t c2 = f2_pack(a.scale_log2, a.scale_log2);
   uint32_t af_par = 0;
   int g = 0;
   bool ok = true;
@@ -877,6 +887,7 @@ __device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32
     const int lo_i = lr[i];
     const int lo_last = lr[q0 + BM - 1];
     const float l2 = a.lse2[rowterm], dl = a.delta[rowterm];
+    const uint64_t nl2 = f2_pack(-l2, -l2), ndl2 = f2_pack(-dl, -dl);
     for (int j = 0; j < n; ++j, ++g) {
       const int k0 = (R.first + j) * BN;
       const uint32_t tY = tmem + lane_off + DQ_COL_Y + uint32_t(g & 1) * 128 + 64 * w;
@@ -899,7 +910,12 @@ __device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->x_free);
 #pragma unroll
-        for (int e = 0; e < 64; ++e) p[e] = ex2_approx(fmaf(__uint_as_float(sv[e]), c, -l2));
+        for (int e = 0; e < 64; e += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nl2), x0, x1);
+          p[e] = ex2_approx(x0);
+          p[e + 1] = ex2_approx(x1);
+        }
       }
       if (!full) {
 #pragma unroll
@@ -925,9 +941,13 @@ __device__ __forceinline__ bool dq_softmax(const BwArgs &a, DqBars *bars, uint32
         }
         uint32_t dk[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          dk[e] = pack_bf16x2(p[ch * 16 + 2 * e] * (__uint_as_float(dv[ch * 16 + 2 * e]) - dl),
-                              p[ch * 16 + 2 * e + 1] * (__uint_as_float(dv[ch * 16 + 2 * e + 1]) - dl));
+        for (int e = 0; e < 8; ++e) {
+          const int q = ch * 16 + 2 * e;
+          float s0, s1;
+          f2_unpack(f2_mul(f2_pack(p[q], p[q + 1]),
+                           f2_add(f2_pack(__uint_as_float(dv[q]), __uint_as_float(dv[q + 1])), ndl2)), s0, s1);
+          dk[e] = pack_bf16x2(s0, s1);
+        }
         tmem_st8(tY + ch * 16, dk);
       }
       tmem_st_wait();
