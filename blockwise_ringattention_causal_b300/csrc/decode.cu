@@ -9,7 +9,9 @@
 // memory with bulk copies (three stages of 8 tokens x 16 heads x 2 tensors, 192 KB, so
 // the SM keeps up to 128 KB of loads in flight), and 16 half-warps, one per head,
 // run the online softmax over the staged tokens: lane l of a half-warp owns dims
-// 8 l .. 8 l + 7, a score is the sum of the 16 lanes' partial dot products. Each CTA
+// 8 l .. 8 l + 7, a score is the sum of the 16 lanes' partial dot products (an xor
+// all-reduce for T = 1, 3; a halving reduce-scatter for T = 2, 4, where the shuffles of
+// the all-reduce, not HBM, set the pace). Each CTA
 // leaves, per (head, query), the running max m, the sum l and the unnormalised output
 // of its split. Kernel 2 merges the splits of each (row, head, query):
 //   M = max m_s,  L = sum_s l_s 2^(m_s - M),  out = sum_s o_s 2^(m_s - M) / L,
@@ -124,99 +126,212 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_split_kernel(const __gr
     __syncwarp();
   } else {
     // ---- consumers: half-warp hw = head h0 + hw; lane l16 owns dims 8 l16 .. 8 l16 + 7
-    const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
-    const int h = h0 + min(hw, nh - 1);   // half-warps past the last head shadow it and store nothing
-    float qf[T][8], o[T][8], m[T], l[T];
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      const uint4 u = a.q[((size_t(b) * a.T + t) * a.H + h) * (HD / 8) + l16];
-      bf16x8_to_f32(u, qf[t]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        qf[t][e] *= a.scale_log2;
-        o[t][e] = 0.f;
-      }
-      m[t] = -__builtin_huge_valf();
-      l[t] = 0.f;
-    }
-    int seen = 0;
-    for (int st = 0; st < n_steps; ++st) {
-      const int slot = st % DEC_NST;
-      if (!(ok = mbar_wait(&bars->full[slot], (st / DEC_NST) & 1, ctl))) break;
-      seen = st + 1;
-      const uint8_t *stage = smem + slot * DEC_STAGE_BYTES + hw * (HD * 2) + l16 * 16;
-      const int j0 = s0 + st * DEC_TB;
-      float s[T][DEC_TB];
-#pragma unroll
-      for (int u = 0; u < DEC_TB; ++u) {
-        float kf[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(stage + u * DEC_TOK_BYTES), kf);
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          float acc = 0.f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc = fmaf(qf[t][e], kf[e], acc);
-          s[t][u] = acc;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < DEC_TB; ++u)
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          float x = s[t][u];
-          x += __shfl_xor_sync(0xffffffffu, x, 8);
-          x += __shfl_xor_sync(0xffffffffu, x, 4);
-          x += __shfl_xor_sync(0xffffffffu, x, 2);
-          x += __shfl_xor_sync(0xffffffffu, x, 1);
-          // query t sits at position len - T + t and sees keys up to it; keys past the
-          // split's end (a partial last stage) are not there
-          const int j = j0 + u;
-          s[t][u] = (j < s1 && j <= len - T + t) ? x : -__builtin_huge_valf();
-        }
-      float p[T][DEC_TB];
+    if constexpr (T % 2 == 0) {
+      // T = 2, 4: the 8 T partial scores of a stage are reduce-scattered over the 16 lanes
+      // (halving exchanges: after the xor-8, -4, -2, -1 steps lane l16 holds the complete
+      // scores of columns VPL l16 .. VPL l16 + VPL - 1, all of query t_l), 30 shuffles
+      // instead of the 4 x 8 T of an all-reduce; each lane takes the softmax of its own
+      // scores, and the P.V step fetches every p from its lane by index.
+      const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
+      const int h = h0 + min(hw, nh - 1);   // half-warps past the last head shadow it and store nothing
+      const int hbase = lane & 16;          // first lane of this half-warp
+      constexpr int N = 8 * T, VPL = N / 16, LPT = 8 / VPL;
+      const int c0 = VPL * l16, t_l = c0 / 8, u_l = c0 % 8;
+      float qf[T][8], o[T][8];
 #pragma unroll
       for (int t = 0; t < T; ++t) {
-        float mx = s[t][0];
+        const uint4 u = a.q[((size_t(b) * a.T + t) * a.H + h) * (HD / 8) + l16];
+        bf16x8_to_f32(u, qf[t]);
 #pragma unroll
-        for (int u = 1; u < DEC_TB; ++u) mx = fmaxf(mx, s[t][u]);
-        const float m_new = fmaxf(m[t], mx);
-        const float m_use = m_new == -__builtin_huge_valf() ? 0.f : m_new;
-        const float alpha = ex2_approx(m[t] - m_use);   // 0 while nothing was visible
-        float sum = 0.f;
+        for (int e = 0; e < 8; ++e) {
+          qf[t][e] *= a.scale_log2;
+          o[t][e] = 0.f;
+        }
+      }
+      float m_l = -__builtin_huge_valf(), l_l = 0.f;   // query t_l: running max, this lane's share of the sum
+      int seen = 0;
+      for (int st = 0; st < n_steps; ++st) {
+        const int slot = st % DEC_NST;
+        if (!(ok = mbar_wait(&bars->full[slot], (st / DEC_NST) & 1, ctl))) break;
+        seen = st + 1;
+        const uint8_t *stage = smem + slot * DEC_STAGE_BYTES + hw * (HD * 2) + l16 * 16;
+        const int j0 = s0 + st * DEC_TB;
+        float v[N];
 #pragma unroll
         for (int u = 0; u < DEC_TB; ++u) {
-          p[t][u] = ex2_approx(s[t][u] - m_use);
-          sum += p[t][u];
+          float kf[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4 *>(stage + u * DEC_TOK_BYTES), kf);
+#pragma unroll
+          for (int t = 0; t < T; ++t) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(qf[t][e], kf[e], acc);
+            v[t * 8 + u] = acc;
+          }
         }
-        l[t] = l[t] * alpha + sum;
-        m[t] = m_new;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[t][e] *= alpha;
+        for (int m = 8, n = N / 2; m >= 1; m >>= 1, n >>= 1) {
+          const bool upper = (l16 & m) != 0;   // keeps the upper half of the remaining columns
+#pragma unroll
+          for (int i = 0; i < n; ++i) {
+            const float send = upper ? v[i] : v[i + n];
+            const float keep = upper ? v[i + n] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          }
+        }
+        // mask: keys past the split's end, or after the query's position len - T + t
+        float mx = -__builtin_huge_valf();
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int j = j0 + u_l + i;
+          if (j >= s1 || j > len - T + t_l) v[i] = -__builtin_huge_valf();
+          mx = fmaxf(mx, v[i]);
+        }
+#pragma unroll
+        for (int d = 1; d < LPT; d <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+        const float m_new = fmaxf(m_l, mx);
+        const float m_use = m_new == -__builtin_huge_valf() ? 0.f : m_new;
+        const float alpha = ex2_approx(m_l - m_use);   // 0 while nothing was visible
+        m_l = m_new;
+        float pl[VPL], psum = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          pl[i] = ex2_approx(v[i] - m_use);
+          psum += pl[i];
+        }
+        l_l = l_l * alpha + psum;
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          const float al = __shfl_sync(0xffffffffu, alpha, hbase + t * LPT);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[t][e] *= al;
+        }
+#pragma unroll
+        for (int u = 0; u < DEC_TB; ++u) {
+          // slots past a partial last stage hold stale bytes (possibly NaN patterns): skip
+          // them rather than multiply them by p = 0 (j0 and s1 are the same for the whole CTA)
+          if (j0 + u >= s1) continue;
+          float vf[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4 *>(stage + (DEC_TB + u) * DEC_TOK_BYTES), vf);
+#pragma unroll
+          for (int t = 0; t < T; ++t) {
+            const int c = t * 8 + u;
+            const float pc = __shfl_sync(0xffffffffu, pl[c % VPL], hbase + c / VPL);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[t][e] = fmaf(pc, vf[e], o[t][e]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->empty[slot]);
       }
+      if (warp == 0 && lane == 0) bars->seen = seen;
 #pragma unroll
-      for (int u = 0; u < DEC_TB; ++u) {
-        // slots past a partial last stage hold stale bytes (possibly NaN patterns): skip
-        // them rather than multiply them by p = 0
-        if (j0 + u >= s1) continue;
-        float vf[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(stage + (DEC_TB + u) * DEC_TOK_BYTES), vf);
+      for (int d = 1; d < LPT; d <<= 1) l_l += __shfl_xor_sync(0xffffffffu, l_l, d);
+      if (ok && hw < nh) {
 #pragma unroll
-        for (int t = 0; t < T; ++t)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[t][e] = fmaf(p[t][u], vf[e], o[t][e]);
+        for (int t = 0; t < T; ++t) {
+          const size_t pi = ((size_t(b) * a.H + h) * a.T + t) * a.n_split + split;
+          float4 *dst = reinterpret_cast<float4 *>(a.part_o + pi * HD + 8 * l16);
+          dst[0] = make_float4(o[t][0], o[t][1], o[t][2], o[t][3]);
+          dst[1] = make_float4(o[t][4], o[t][5], o[t][6], o[t][7]);
+        }
+        if (u_l == 0) a.part_ml[((size_t(b) * a.H + h) * a.T + t_l) * a.n_split + split] = make_float2(m_l, l_l);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->empty[slot]);
-    }
-    if (warp == 0 && lane == 0) bars->seen = seen;
-    if (ok && hw < nh) {
-#pragma unroll
+    } else {
+      const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
+      const int h = h0 + min(hw, nh - 1);   // half-warps past the last head shadow it and store nothing
+      float qf[T][8], o[T][8], m[T], l[T];
+  #pragma unroll
       for (int t = 0; t < T; ++t) {
-        const size_t pi = ((size_t(b) * a.H + h) * a.T + t) * a.n_split + split;
-        float4 *dst = reinterpret_cast<float4 *>(a.part_o + pi * HD + 8 * l16);
-        dst[0] = make_float4(o[t][0], o[t][1], o[t][2], o[t][3]);
-        dst[1] = make_float4(o[t][4], o[t][5], o[t][6], o[t][7]);
-        if (l16 == 0) a.part_ml[pi] = make_float2(m[t], l[t]);
+        const uint4 u = a.q[((size_t(b) * a.T + t) * a.H + h) * (HD / 8) + l16];
+        bf16x8_to_f32(u, qf[t]);
+  #pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          qf[t][e] *= a.scale_log2;
+          o[t][e] = 0.f;
+        }
+        m[t] = -__builtin_huge_valf();
+        l[t] = 0.f;
+      }
+      int seen = 0;
+      for (int st = 0; st < n_steps; ++st) {
+        const int slot = st % DEC_NST;
+        if (!(ok = mbar_wait(&bars->full[slot], (st / DEC_NST) & 1, ctl))) break;
+        seen = st + 1;
+        const uint8_t *stage = smem + slot * DEC_STAGE_BYTES + hw * (HD * 2) + l16 * 16;
+        const int j0 = s0 + st * DEC_TB;
+        float s[T][DEC_TB];
+  #pragma unroll
+        for (int u = 0; u < DEC_TB; ++u) {
+          float kf[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4 *>(stage + u * DEC_TOK_BYTES), kf);
+  #pragma unroll
+          for (int t = 0; t < T; ++t) {
+            float acc = 0.f;
+  #pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(qf[t][e], kf[e], acc);
+            s[t][u] = acc;
+          }
+        }
+  #pragma unroll
+        for (int u = 0; u < DEC_TB; ++u)
+  #pragma unroll
+          for (int t = 0; t < T; ++t) {
+            float x = s[t][u];
+            x += __shfl_xor_sync(0xffffffffu, x, 8);
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            x += __shfl_xor_sync(0xffffffffu, x, 2);
+            x += __shfl_xor_sync(0xffffffffu, x, 1);
+            // query t sits at position len - T + t and sees keys up to it; keys past the
+            // split's end (a partial last stage) are not there
+            const int j = j0 + u;
+            s[t][u] = (j < s1 && j <= len - T + t) ? x : -__builtin_huge_valf();
+          }
+        float p[T][DEC_TB];
+  #pragma unroll
+        for (int t = 0; t < T; ++t) {
+          float mx = s[t][0];
+  #pragma unroll
+          for (int u = 1; u < DEC_TB; ++u) mx = fmaxf(mx, s[t][u]);
+          const float m_new = fmaxf(m[t], mx);
+          const float m_use = m_new == -__builtin_huge_valf() ? 0.f : m_new;
+          const float alpha = ex2_approx(m[t] - m_use);   // 0 while nothing was visible
+          float sum = 0.f;
+  #pragma unroll
+          for (int u = 0; u < DEC_TB; ++u) {
+            p[t][u] = ex2_approx(s[t][u] - m_use);
+            sum += p[t][u];
+          }
+          l[t] = l[t] * alpha + sum;
+          m[t] = m_new;
+  #pragma unroll
+          for (int e = 0; e < 8; ++e) o[t][e] *= alpha;
+        }
+  #pragma unroll
+        for (int u = 0; u < DEC_TB; ++u) {
+          // slots past a partial last stage hold stale bytes (possibly NaN patterns): skip
+          // them rather than multiply them by p = 0
+          if (j0 + u >= s1) continue;
+          float vf[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4 *>(stage + (DEC_TB + u) * DEC_TOK_BYTES), vf);
+  #pragma unroll
+          for (int t = 0; t < T; ++t)
+  #pragma unroll
+            for (int e = 0; e < 8; ++e) o[t][e] = fmaf(p[t][u], vf[e], o[t][e]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->empty[slot]);
+      }
+      if (warp == 0 && lane == 0) bars->seen = seen;
+      if (ok && hw < nh) {
+  #pragma unroll
+        for (int t = 0; t < T; ++t) {
+          const size_t pi = ((size_t(b) * a.H + h) * a.T + t) * a.n_split + split;
+          float4 *dst = reinterpret_cast<float4 *>(a.part_o + pi * HD + 8 * l16);
+          dst[0] = make_float4(o[t][0], o[t][1], o[t][2], o[t][3]);
+          dst[1] = make_float4(o[t][4], o[t][5], o[t][6], o[t][7]);
+          if (l16 == 0) a.part_ml[pi] = make_float2(m[t], l[t]);
+        }
       }
     }
   }
